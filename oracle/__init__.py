@@ -1,0 +1,21 @@
+"""Plain fp64 CPU oracle for absorbed-MLA decode attention.
+
+TEST INFRASTRUCTURE ONLY.  Nothing in the product path (the CUDA library, its
+Python binding, the timed legs of the benchmark) may import or call this
+package; only the test-suite, the smoke check and the benchmark's CPU-baseline
+and reference legs do.  It shares no code with the GPU implementation.
+"""
+
+from .mla_oracle import (  # noqa: F401
+    D_QK,
+    D_V,
+    PAGE,
+    attend,
+    bf16_bits_to_f64,
+    combine,
+    f64_to_bf16_bits,
+    mla_decode,
+    physical_rows,
+    softmax_weights,
+    visible_positions,
+)

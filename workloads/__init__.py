@@ -1,0 +1,194 @@
+"""Seeded synthetic inputs for MLA decode: the one module both sides share.
+
+This module only draws random inputs; it holds none of the attention
+arithmetic.  The CUDA path and the CPU oracle are both fed from it.
+
+Shapes follow the decode workloads the pages describe: 128 weight-absorbed
+query heads of 576 dims (512 latent + 64 RoPE), one 576-dim bf16 latent row
+per cached token, 64-token pages in a shared pool reached through a block
+table ("DeepSeek V3/R1 Inference Efficiency (2)", §2.4.1, decode shapes;
+"How DeepSeek Inference Works", levers table, "KV-cache layout (MLA,
+paging)").  Batch points 32/64/80/128 mirror the pages' decode batch sizes
+(b = 64 per microbatch in §2.4; batch 32 and 80 in "The Premise That
+Wasn't").
+
+Structure (lengths, page permutations, top-k lists, pad counts, spiked rows)
+comes from numpy's Philox generator keyed by (seed, stream id), so it is the
+same on every machine.  The N(0,1) values come from torch's generator on the
+target device, drawn in fixed-size chunks, so a run is reproducible on one
+device; both sides of a parity test read the same bytes.
+"""
+
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import numpy as np
+import torch
+
+H = 128
+D_QK = 576
+D_V = 512
+PAGE = 64
+SCALE = 1.0 / math.sqrt(192.0)  # 1/sqrt(d + r), d = 128, r = 64
+
+_CHUNK_ELEMS = 1 << 26  # elements drawn per randn call
+
+
+@dataclasses.dataclass
+class Workload:
+    name: str
+    q: torch.Tensor  # bf16 [B, s_q, H, 576]
+    kv: torch.Tensor  # bf16 [num_pages, 64, 576]
+    block_table: torch.Tensor  # int32 [B, max_pages]
+    cache_lens: torch.Tensor  # int32 [B]
+    topk_idx: torch.Tensor | None  # int32 [B, s_q, k] or None
+    softmax_scale: float
+    causal: bool
+
+    @property
+    def batch(self) -> int:
+        return self.q.shape[0]
+
+    @property
+    def s_q(self) -> int:
+        return self.q.shape[1]
+
+    @property
+    def num_pages(self) -> int:
+        return self.kv.shape[0]
+
+    @property
+    def topk(self) -> int:
+        return 0 if self.topk_idx is None else self.topk_idx.shape[-1]
+
+
+def _np_rng(seed: int, stream: int) -> np.random.Generator:
+    return np.random.Generator(np.random.Philox(np.random.SeedSequence([seed, stream])))
+
+
+def _randn_bf16(shape, seed: int, stream: int, device) -> torch.Tensor:
+    """N(0,1) rounded to bf16, drawn in fixed chunks on `device`."""
+    out = torch.empty(shape, dtype=torch.bfloat16, device=device)
+    flat = out.view(-1)
+    g = torch.Generator(device=device)
+    g.manual_seed(seed * 1000003 + stream)
+    n = flat.numel()
+    for lo in range(0, n, _CHUNK_ELEMS):
+        hi = min(n, lo + _CHUNK_ELEMS)
+        flat[lo:hi] = torch.randn(hi - lo, generator=g, device=device,
+                                  dtype=torch.float32).to(torch.bfloat16)
+    return out
+
+
+def make_workload(name: str, lens, s_q: int = 1, causal: bool = False, *,
+                  topk: int = 0, pad_range=(0, 0), spike_frac: float = 0.0,
+                  shuffle: bool = True, extra_pages: int = 0, seed: int = 0,
+                  device="cpu", max_pages: int | None = None) -> Workload:
+    """Build one decode call's inputs.
+
+    lens:        per-request cache lengths (tokens).
+    topk:        if > 0, each (request, token) gets a sorted list of
+                 topk - pad distinct positions drawn uniformly from
+                 [0, len), followed by pad entries of -1, pad ~ U{pad_range}.
+    spike_frac:  fraction of pool rows multiplied by 8 (exact in bf16).
+    shuffle:     pages of all requests are placed in the pool in a seeded
+                 random order; otherwise request b's pages are contiguous.
+    extra_pages: unused pool pages appended (filled with data too).
+    max_pages:   width of the block table; unused entries hold -1.
+    """
+    lens = np.asarray(lens, dtype=np.int64)
+    B = lens.size
+    npages_req = (lens + PAGE - 1) // PAGE
+    total = int(npages_req.sum()) + int(extra_pages)
+    width = int(max(1, npages_req.max() if B else 1)) if max_pages is None else int(max_pages)
+    rng = _np_rng(seed, 1)
+    order = rng.permutation(total) if shuffle else np.arange(total)
+    table = np.full((B, width), -1, dtype=np.int32)
+    cursor = 0
+    for b in range(B):
+        n = int(npages_req[b])
+        table[b, :n] = order[cursor:cursor + n]
+        cursor += n
+
+    q = _randn_bf16((B, s_q, H, D_QK), seed, 2, device)
+    kv = _randn_bf16((max(total, 1), PAGE, D_QK), seed, 3, device)
+    if spike_frac > 0:
+        rows = np.nonzero(_np_rng(seed, 4).random(kv.shape[0] * PAGE) < spike_frac)[0]
+        idx = torch.from_numpy(rows).to(device)
+        flat = kv.view(-1, D_QK)
+        flat[idx] = flat[idx] * 8
+
+    topk_t = None
+    if topk > 0:
+        rng_k = _np_rng(seed, 5)
+        lo, hi = pad_range
+        idx = np.full((B, s_q, topk), -1, dtype=np.int32)
+        for b in range(B):
+            for t in range(s_q):
+                pad = int(rng_k.integers(lo, hi + 1)) if hi > lo else int(lo)
+                n = max(0, min(topk - pad, int(lens[b])))
+                pos = np.sort(rng_k.choice(int(lens[b]), size=n, replace=False))
+                idx[b, t, :n] = pos
+        topk_t = torch.from_numpy(idx).to(device)
+
+    return Workload(
+        name=name, q=q, kv=kv,
+        block_table=torch.from_numpy(table).to(device),
+        cache_lens=torch.from_numpy(lens.astype(np.int32)).to(device),
+        topk_idx=topk_t, softmax_scale=SCALE, causal=causal)
+
+
+# The five decode workloads (full sizes).
+CONFIGS = ("single", "uniform_b32", "mtp_b64", "long_b128", "sparse_b80")
+
+
+def make_config(name: str, seed: int = 0, device="cpu", batch: int | None = None,
+                length: int | None = None) -> Workload:
+    """One of the five named workloads; `batch` / `length` shrink it for tests.
+
+    single       B=1, L=256 (4 pages, identity block table), s_q=1
+    uniform_b32  B=32, every L=4096, shuffled pool
+    mtp_b64      B=64, s_q=2 causal, L ~ U{1..8192}, shuffled pool, table
+                 entries past each request's pages = -1
+    long_b128    B=128, every L=32768, 5% of pool rows scaled x8
+    sparse_b80   B=80, every L=65536, top-2048 sorted distinct positions with
+                 the last 0..300 entries padded with -1
+    """
+    if name == "single":
+        return make_workload(name, [length or 256], shuffle=False, seed=seed, device=device)
+    if name == "uniform_b32":
+        B = batch or 32
+        return make_workload(name, [length or 4096] * B, seed=seed, device=device)
+    if name == "mtp_b64":
+        B = batch or 64
+        top = length or 8192
+        lens = _np_rng(seed, 6).integers(1, top + 1, size=B)
+        return make_workload(name, lens, s_q=2, causal=True, seed=seed, device=device,
+                             max_pages=(top + PAGE - 1) // PAGE)
+    if name == "long_b128":
+        B = batch or 128
+        return make_workload(name, [length or 32768] * B, spike_frac=0.05, seed=seed,
+                             device=device)
+    if name == "sparse_b80":
+        B = batch or 80
+        L = length or 65536
+        k = min(2048, L)
+        return make_workload(name, [L] * B, topk=k, pad_range=(0, min(300, k)),
+                             seed=seed, device=device)
+    raise KeyError(name)
+
+
+def bf16_bits(t: torch.Tensor) -> np.ndarray:
+    """Host copy of a bf16 tensor as raw uint16 bit patterns."""
+    return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def host_arrays(w: Workload):
+    """The workload as numpy arrays (bf16 as uint16 bits) for the oracle."""
+    return dict(
+        q_bits=bf16_bits(w.q), kv_bits=bf16_bits(w.kv),
+        block_table=w.block_table.cpu().numpy(), cache_lens=w.cache_lens.cpu().numpy(),
+        softmax_scale=w.softmax_scale, causal=w.causal,
+        topk_idx=None if w.topk_idx is None else w.topk_idx.cpu().numpy())
