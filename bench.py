@@ -1,0 +1,381 @@
+"""Benchmark of one MLA decode step (plan + attention + combine) on GB300.
+
+Default workload: the B=64 variable-length two-token (MTP, causal) decode
+step - 64 requests, cache lengths ~U{1..8192}, 128 heads x 576 dims, 64-token
+pages in a shuffled pool, bf16 inputs ~N(0,1) - the batch-64 decode shape
+the pages quote (b = 64 per microbatch).  Inputs are synthetic and resident
+in HBM; the pool exceeds L2 and L2 is also flushed (256 MB write) before
+every timed step.
+
+Prints ONE JSON line.  `value` is the whole-job attention throughput in
+TFLOP/s (algorithmic FLOPs of every rank's steps / max-over-ranks time);
+microseconds per call, HBM GB/s and the roofline fractions ride along.
+`--impl reference` times the fp64 CPU oracle instead (rank 0 only).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MLA decode us/call, TFLOPS and HBM GB/s as % of GB300 roofline (B=64)"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+DECODE_SOURCES = ["decode_kernel.cu", "ptx.cuh", "common.cuh", "plan.cuh"]
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for f in DECODE_SOURCES:
+        h.update(open(os.path.join(ROOT, "mla_latent_kv_09_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(workload: str):
+    """DRAM bytes per decode launch from a committed ncu capture, if it was
+    taken on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    if not os.path.exists(path):
+        return None
+    d = json.load(open(path))
+    e = d.get(workload)
+    if not e or e.get("kernel_hash") != kernel_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        self.proc.wait()
+        self.f.close()
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = max(mx, float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        if backend == "nccl":
+            import torch
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def oracle_sample(w, host, reqs):
+    """Run the fp64 oracle on requests `reqs` (all their query tokens)."""
+    import oracle
+    sel = [(b, t) for b in reqs for t in range(w.s_q)]
+    oracle.mla_decode(host["q_bits"], host["kv_bits"], host["block_table"], host["cache_lens"],
+                      host["softmax_scale"], causal=host["causal"], topk_idx=host["topk_idx"], select=sel)
+
+
+def sample_flops(w, host, reqs):
+    from mla_latent_kv_09_gb300 import accounting as acc
+    import numpy as np
+    counts = acc.visible_counts(host["cache_lens"], w.s_q, w.causal, host["topk_idx"])
+    return int(np.asarray(counts)[list(reqs)].sum()) * acc.FLOPS_PER_QT
+
+
+def cpu_baseline(w, host, budget_s: float):
+    """The oracle timed on this host's cores over a bounded sample of the
+    workload: whole requests, in order, until about budget_s seconds."""
+    reqs, t0 = [], time.perf_counter()
+    for b in range(w.batch):
+        oracle_sample(w, host, [b])
+        reqs.append(b)
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    fl = sample_flops(w, host, reqs)
+    return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{len(reqs)} of {w.batch} requests (all {w.s_q} query tokens each), "
+                      f"{dt:.1f} s, numpy fp64 with BLAS on all host cores"}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    import workloads as wl
+    w = wl.make_config(args.config, device="cpu")
+    host = wl.host_arrays(w)
+    order = list(range(w.batch))
+    for i in range(args.warmup):
+        oracle_sample(w, host, [order[i % w.batch]])
+    times, flops = [], 0
+    t_all = time.perf_counter()
+    for i in range(args.steps):
+        b = order[i % w.batch]
+        t0 = time.perf_counter()
+        oracle_sample(w, host, [b])
+        times.append(time.perf_counter() - t0)
+        flops += sample_flops(w, host, [b])
+    dt = time.perf_counter() - t_all
+    val = flops / dt / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": args.config, "batch": w.batch, "s_q": w.s_q, "heads": 128,
+                       "d_qk": 576, "d_v": 512, "page": 64, "causal": w.causal,
+                       "step": "one request (all query tokens) of the workload per step"},
+            "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": f"{args.steps} steps of one request each, cycling through "
+                                       f"the {w.batch} requests"},
+            "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, world, rank, local):
+    import torch
+
+    import mla_latent_kv_09_gb300 as m
+    import workloads as wl
+    from mla_latent_kv_09_gb300 import accounting as acc
+    from mla_latent_kv_09_gb300 import build as mbuild
+
+    mbuild.build()
+    m.load()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = wl.make_config(args.config, seed=args.seed + rank, device=dev)
+    B, s_q = w.batch, w.s_q
+    host_lens = w.cache_lens.cpu().numpy()
+    host_topk = None if w.topk_idx is None else w.topk_idx.cpu().numpy()
+    flops = acc.step_flops(host_lens, s_q, w.causal, host_topk)
+    nbytes = acc.step_bytes(host_lens, s_q, w.causal, host_topk)
+    pk, pk_kind = peaks()
+    ridge = pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)
+    bound = "tensor" if flops / nbytes > ridge else "hbm"
+
+    ws = m.Workspace(B, s_q, args.num_units, dev)
+    out = torch.empty((B, s_q, 128, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, s_q, 128), dtype=torch.float32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    topk = w.topk
+    flags = m.MLA_FLAG_CAUSAL if w.causal else 0
+    U = ws.num_units
+
+    def plan():
+        m.mla_decode_plan(w.cache_lens, B, s_q, topk, U, ws.buf, ws.nbytes, stream)
+
+    def decode():
+        m.mla_decode(w.q, w.kv, w.num_pages, w.block_table, w.block_table.stride(0), w.cache_lens, B, s_q,
+                     128, w.softmax_scale, w.topk_idx, topk, flags, U, ws.buf, ws.nbytes, out, lse, stream)
+
+    def combine():
+        m.mla_combine(ws.buf, ws.nbytes, B, s_q, 128, flags, U, out, lse, stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        plan(); decode(); combine()
+    torch.cuda.synchronize()
+    status = m.mla_workspace_status(ws.buf, stream.cuda_stream)
+    if status != 0:
+        raise RuntimeError(f"device status after warm-up: {m.mla_status_string(status)}")
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        e = ev[i]
+        e[0].record(stream)
+        plan()
+        e[1].record(stream)
+        decode()
+        e[2].record(stream)
+        combine()
+        e[3].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    wall = time.perf_counter() - t_wall
+    clocks = sampler.stop()
+    step_ms = sum(e[0].elapsed_time(e[3]) for e in ev) / args.steps
+    dec_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / args.steps
+    plan_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps
+    comb_ms = sum(e[2].elapsed_time(e[3]) for e in ev) / args.steps
+    step_ms_max = max_over_ranks(step_ms, world)
+    value = world * flops / (step_ms_max * 1e-3) / 1e12
+
+    # end to end through the host-buffer API: inputs copied in, O/LSE copied out, every step
+    e2e = None
+    if not args.no_e2e:
+        pin = {k: t.cpu().pin_memory() for k, t in
+               [("q", w.q), ("kv_cache", w.kv), ("block_table", w.block_table), ("cache_lens", w.cache_lens)]
+               + ([("topk_idx", w.topk_idx)] if w.topk_idx is not None else [])}
+        dbuf = {"q": w.q, "kv_cache": w.kv, "block_table": w.block_table, "cache_lens": w.cache_lens,
+                "topk_idx": w.topk_idx, "out": out, "lse": lse}
+        o_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        l_h = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+        h2d = sum(t.numel() * t.element_size() for t in pin.values())
+        d2h = o_h.numel() * o_h.element_size() + l_h.numel() * l_h.element_size()
+        n_e2e = max(3, min(args.steps, args.e2e_steps))
+
+        def e2e_step():
+            m.decode_step_host(pin["q"], pin["kv_cache"], pin["block_table"], pin["cache_lens"],
+                               w.softmax_scale, device=dev, causal=w.causal, topk_idx=pin.get("topk_idx"),
+                               workspace=ws, dev_buffers=dbuf, out_host=o_h, lse_host=l_h)
+
+        for _ in range(3):
+            e2e_step()
+        barrier(world)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            e2e_step()
+        torch.cuda.synchronize()
+        dt = max_over_ranks((time.perf_counter() - t0) / n_e2e, world)
+        e2e = {"value": world * flops / dt / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "steps": n_e2e, "ms_per_step": 1e3 * dt}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        host = wl.host_arrays(w)
+        cpu = cpu_baseline(w, host, args.cpu_budget)
+
+    if rank != 0:
+        return
+    dec_s = dec_ms * 1e-3
+    if bound == "tensor":
+        achieved, peak, unit = flops / dec_s / 1e12, pk["bf16_tflops"], "TFLOP/s"
+    else:
+        achieved, peak, unit = nbytes / dec_s / 1e9, pk["hbm_gbs"], "GB/s"
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_ms_max, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.config, "batch": B, "s_q": s_q, "heads": 128, "d_qk": 576, "d_v": 512,
+                   "page": 64, "causal": w.causal, "topk": topk, "num_units": U,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "256 MB L2 flush before every timed step; cache pool exceeds L2",
+                   "algorithmic_gflop": flops / 1e9, "algorithmic_mb": nbytes / 1e6},
+        "us_per_call": step_ms_max * 1e3,
+        "us_decode_kernel": dec_ms * 1e3, "us_plan": plan_ms * 1e3, "us_combine": comb_ms * 1e3,
+        "tflops": flops / (step_ms * 1e-3) / 1e12,
+        "hbm_gbs": nbytes / (step_ms * 1e-3) / 1e9,
+        "frac_tensor_peak": flops / (step_ms * 1e-3) / 1e12 / pk["bf16_tflops"],
+        "frac_hbm_peak": nbytes / (step_ms * 1e-3) / 1e9 / pk["hbm_gbs"],
+        "frac_roofline": max(flops / (pk["bf16_tflops"] * 1e12), nbytes / (pk["hbm_gbs"] * 1e9))
+                         / (step_ms * 1e-3),
+        "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+                     "frac": achieved / peak, "traffic": measured_traffic(args.config),
+                     "kernel": "mla_decode_kernel", "peak_source": f"{pk_kind} (burst)"},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "wall_s_timed_region": wall,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="mtp_b64")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--num-units", type=int, default=0)
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

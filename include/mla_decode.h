@@ -1,0 +1,188 @@
+/*
+ * mla_decode.h — C ABI of the GB300 (sm_103a) MLA decode library.
+ *
+ * The operation
+ * -------------
+ * Weight-absorbed multi-head latent attention at decode time ("DeepSeek
+ * V3/R1 Inference Efficiency (2): Reverse-Engineering the Production
+ * Deployment", §2.4.1, Compute, "MLA/MQA attention"): each of a request's
+ * 128 query heads carries 576 dims (512 latent + 64 RoPE) and attends, in MQA
+ * form, over the request's cached latent rows (576 bf16 per token).  The
+ * score contraction spans all 576 dims, the value is the first 512 dims of
+ * the same row.  For request b, query token t and head h:
+ *
+ *     s_j = scale * <q[b,t,h,:], kv[row(j),:]>          j visible
+ *     O[b,t,h,:] = sum_j softmax(s)_j * kv[row(j), 0:512]
+ *     LSE[b,t,h] = ln sum_j exp(s_j)                      (natural log)
+ *
+ * The cache lives in 64-token pages of a shared pool reached through a block
+ * table ("How DeepSeek Inference Works", levers table, "KV-cache layout (MLA,
+ * paging)"): logical position j of request b is pool row
+ * block_table[b * bt_stride + j / 64] * 64 + j % 64.
+ *
+ * Long or skewed lengths are split across the GPU (split-KV, the split-K
+ * remedy of "The 31-Millisecond Smoking Gun" and the wave-quantisation
+ * discussion of "The Premise That Wasn't", Wave-Aware NSPLIT); partial
+ * results are merged with LSE weights.
+ *
+ * Three calls make one decode step, all asynchronous on `stream`:
+ *     mla_decode_plan  -> partitions the (request, 64-token tile) work
+ *     mla_decode       -> attention; writes final O/LSE for unsplit requests
+ *                         and fp32 partials for split ones
+ *     mla_combine      -> merges the partials, writes O/LSE of split requests
+ *                         and of requests with nothing to attend to
+ *
+ * Conventions
+ * -----------
+ *  - Every pointer is a DEVICE pointer unless stated otherwise.  The caller
+ *    owns all memory; the library allocates nothing.
+ *  - The return value reports errors detectable on the host (bad arguments,
+ *    unsupported shapes or device, launch failures).  No call synchronises
+ *    the stream, except mla_decode with MLA_FLAG_VALIDATE.
+ *  - Fixed shapes: 128 query heads, 576 q/k dims, 512 value dims, 64-token
+ *    pages.  Anything else returns MLA_ERR_UNSUPPORTED.  The device must be
+ *    compute capability 10.3 (GB300); there is no other code path.
+ *  - The plan lives in the caller's workspace; the three calls of one step
+ *    must use the same workspace, batch, s_q, topk and num_units.
+ *  - Calls are stateless and thread-safe for distinct workspaces.
+ */
+#ifndef MLA_DECODE_H_
+#define MLA_DECODE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Opaque CUDA stream (cudaStream_t); NULL means the legacy default stream. */
+typedef void* mla_stream_t;
+
+typedef enum {
+  MLA_OK = 0,
+  MLA_ERR_INVALID_ARG = 1,  /* null pointer, negative size, misalignment   */
+  MLA_ERR_UNSUPPORTED = 2,  /* head count / dims / device not supported     */
+  MLA_ERR_WORKSPACE = 3,    /* workspace too small                          */
+  MLA_ERR_CUDA = 4,         /* a CUDA runtime or driver call failed         */
+  MLA_ERR_DEVICE = 5,       /* no sm_103 device current                     */
+  MLA_ERR_BAD_TABLE = 6,    /* validate mode: block-table entry / length out of range */
+  MLA_ERR_BAD_INDEX = 7,    /* validate mode: top-k index outside [-1, len) */
+  MLA_ERR_TIMEOUT = 8       /* a device-side wait ran out (kernel bailed out) */
+} mla_status;
+
+enum {
+  MLA_FLAG_CAUSAL = 1,   /* s_q = 2 MTP decode: token t sees [0, len - s_q + t] */
+  MLA_FLAG_OUT_FP32 = 2, /* O is written as fp32 instead of bf16           */
+  MLA_FLAG_VALIDATE = 4  /* check table / lengths / indices first (syncs)   */
+};
+
+enum { MLA_NUM_HEADS = 128, MLA_D_QK = 576, MLA_D_V = 512, MLA_PAGE = 64 };
+
+/*
+ * Number of persistent work units (one unit = one pair of SMs working as a
+ * 2-CTA cluster) per query token that `num_units = 0` selects on the current
+ * device: the number of co-resident 2-CTA clusters divided by s_q.
+ * Host-only; returns 0 and sets *err on failure (err may be NULL).
+ */
+int mla_default_num_units(int s_q, int* err);
+
+/*
+ * Bytes of workspace the three calls need.  Pure host arithmetic.
+ *   batch      requests (>= 1)
+ *   s_q        query tokens per request (1 or 2)
+ *   num_heads  must be 128
+ *   num_units  work units per query token; 0 = mla_default_num_units(s_q)
+ * Returns 0 on invalid arguments.
+ */
+size_t mla_decode_workspace_size(int batch, int s_q, int num_heads, int num_units);
+
+/*
+ * Split-KV partition of one decode step.  Launches one CTA; reads
+ * cache_lens on the device, so no host synchronisation is needed.
+ *   cache_lens  int32 [batch], tokens in each request's cache (>= 0)
+ *   topk        0 for dense attention; else the length of each top-k list
+ *               (every request then has ceil(topk / 64) tiles)
+ *   num_units   as for mla_decode_workspace_size
+ *   workspace   device buffer of ws_bytes >= mla_decode_workspace_size(...)
+ * The work of request b is ceil(len_b / 64) tiles of 64 tokens; the tiles
+ * of all requests, each request charged a fixed per-split overhead, are cut
+ * into num_units contiguous, equally loaded ranges.  Requests that straddle
+ * a cut are "split" and finish in mla_combine.
+ */
+int mla_decode_plan(const int32_t* cache_lens, int batch, int s_q, int topk,
+                    int num_units, void* workspace, size_t ws_bytes,
+                    mla_stream_t stream);
+
+/*
+ * The same partition computed on the host from host-resident lengths, for
+ * inspection and testing.  Writes, per unit u, unit_meta[5u .. 5u+4] =
+ * {begin_req, begin_tile, end_req, end_tile, first_split} (ranges are
+ * half-open in (request, tile) order), and per request b,
+ * req_meta[4b .. 4b+3] = {n_tiles, n_splits, first_slot, cost_prefix}.
+ * unit_meta holds 5 * num_units ints and req_meta 4 * batch ints (host
+ * memory, caller-owned).  num_units must be >= 1 here.
+ */
+int mla_decode_plan_host(const int32_t* cache_lens_host, int batch, int topk,
+                         int num_units, int32_t* unit_meta, int32_t* req_meta);
+
+/*
+ * Attention for one decode step (after mla_decode_plan on the same stream).
+ *   q            bf16 [batch, s_q, 128, 576], contiguous, 16-B aligned
+ *   kv_cache     bf16 [num_pages, 64, 576], contiguous, 16-B aligned
+ *   num_pages    pages in the pool (rows = 64 * num_pages)
+ *   block_table  int32, row b at block_table + b * bt_stride; entries
+ *                0 .. ceil(len_b / 64) - 1 are read
+ *   bt_stride    elements between block-table rows (>= ceil(max len / 64))
+ *   cache_lens   int32 [batch]
+ *   s_q          1, or 2 (with MLA_FLAG_CAUSAL for MTP decode)
+ *   num_heads    must be 128
+ *   softmax_scale  multiplies the 576-dim dot product (used as float32)
+ *   topk_idx     NULL for dense attention; else int32 [batch, s_q, topk] of
+ *                logical positions in the request's sequence, -1 = unused
+ *                slot; each list attends to exactly its entries (CAUSAL is
+ *                then ignored)
+ *   flags        MLA_FLAG_*
+ *   workspace    the planned workspace
+ *   out          [batch, s_q, 128, 512], bf16 (or fp32 with OUT_FP32)
+ *   lse          fp32 [batch, s_q, 128], natural log; -inf where nothing
+ *                is visible (O is then 0)
+ * Out-of-range table entries or indices never fault: dense page loads
+ * outside the pool read zeros, sparse rows outside it are skipped; results
+ * for such requests are meaningless.  MLA_FLAG_VALIDATE detects them
+ * first: it runs a check kernel, synchronises the stream and returns
+ * MLA_ERR_BAD_TABLE / MLA_ERR_BAD_INDEX without launching the attention.
+ * A device-side wait that runs out (about 2 s) makes the kernel record
+ * MLA_ERR_TIMEOUT in the workspace and return; mla_workspace_status reads it.
+ */
+int mla_decode(const void* q, const void* kv_cache, int64_t num_pages,
+               const int32_t* block_table, int64_t bt_stride,
+               const int32_t* cache_lens, int batch, int s_q, int num_heads,
+               float softmax_scale, const int32_t* topk_idx, int topk,
+               unsigned flags, int num_units, void* workspace, size_t ws_bytes,
+               void* out, float* lse, mla_stream_t stream);
+
+/*
+ * Merge the split requests' partials (LSE = ln sum_s exp(lse_s),
+ * O = sum_s exp(lse_s - LSE) * O_s) and write O = 0, LSE = -inf for
+ * requests with nothing to attend to.  flags: MLA_FLAG_OUT_FP32 as above.
+ */
+int mla_combine(void* workspace, size_t ws_bytes, int batch, int s_q,
+                int num_heads, unsigned flags, int num_units, void* out,
+                float* lse, mla_stream_t stream);
+
+/*
+ * Synchronise `stream` and return the device-side status recorded in the
+ * workspace (MLA_OK, MLA_ERR_TIMEOUT, or a plan overflow as
+ * MLA_ERR_WORKSPACE).
+ */
+int mla_workspace_status(const void* workspace, mla_stream_t stream);
+
+/* Human-readable name of a status code (static string). */
+const char* mla_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_DECODE_H_ */

@@ -1,0 +1,122 @@
+"""GB300 (sm_103a) weight-absorbed MLA decode over a paged latent KV cache.
+
+The computation lives in libmla_decode.so (CUDA, hand-written tcgen05/TMA
+kernels); this package is its Python face:
+
+  * the C-ABI entry points under their C names (mla_decode_plan, mla_decode,
+    mla_combine, ...) taking raw pointers or torch tensors;
+  * `decode_step`, which allocates the outputs and runs plan -> decode ->
+    combine on the current stream;
+  * `decode_step_host`, the same call for host-resident inputs (copies in,
+    runs, copies the outputs back).
+
+PyTorch is used only to allocate device memory and to name streams.
+"""
+
+from __future__ import annotations
+
+from ._binding import (  # noqa: F401
+    MLA_ERR_BAD_INDEX,
+    MLA_ERR_BAD_TABLE,
+    MLA_ERR_CUDA,
+    MLA_ERR_DEVICE,
+    MLA_ERR_INVALID_ARG,
+    MLA_ERR_TIMEOUT,
+    MLA_ERR_UNSUPPORTED,
+    MLA_ERR_WORKSPACE,
+    MLA_FLAG_CAUSAL,
+    MLA_FLAG_OUT_FP32,
+    MLA_FLAG_VALIDATE,
+    MLA_OK,
+    SIGNATURES,
+    MlaError,
+    load,
+    mla_combine,
+    mla_decode,
+    mla_decode_plan,
+    mla_decode_plan_host,
+    mla_decode_workspace_size,
+    mla_default_num_units,
+    mla_status_string,
+    mla_workspace_status,
+)
+
+NUM_HEADS = 128
+D_QK = 576
+D_V = 512
+PAGE = 64
+
+
+class Workspace:
+    """A device workspace sized for (batch, s_q, num_units)."""
+
+    def __init__(self, batch: int, s_q: int, num_units: int = 0, device=None):
+        import torch
+        self.batch, self.s_q = batch, s_q
+        self.num_units = num_units or mla_default_num_units(s_q)
+        self.nbytes = mla_decode_workspace_size(batch, s_q, NUM_HEADS, self.num_units)
+        self.buf = torch.empty(self.nbytes, dtype=torch.uint8, device=device or "cuda")
+
+
+def decode_step(q, kv_cache, block_table, cache_lens, softmax_scale: float, *, causal: bool = False,
+                topk_idx=None, out_fp32: bool = False, validate: bool = False, num_units: int = 0,
+                workspace: Workspace | None = None, out=None, lse=None, stream=None):
+    """One MLA decode step on device tensors: plan, attention, combine.
+
+    q [B, s_q, 128, 576] bf16; kv_cache [num_pages, 64, 576] bf16;
+    block_table [B, W] int32; cache_lens [B] int32; topk_idx [B, s_q, k]
+    int32 or None.  Returns (O [B, s_q, 128, 512] bf16 or fp32, LSE fp32).
+    """
+    import torch
+    B, s_q = q.shape[0], q.shape[1]
+    if workspace is None:
+        workspace = Workspace(B, s_q, num_units, q.device)
+    U = workspace.num_units
+    if out is None:
+        out = torch.empty((B, s_q, NUM_HEADS, D_V), dtype=torch.float32 if out_fp32 else torch.bfloat16,
+                          device=q.device)
+    if lse is None:
+        lse = torch.empty((B, s_q, NUM_HEADS), dtype=torch.float32, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    topk = 0 if topk_idx is None else topk_idx.shape[-1]
+    flags = (MLA_FLAG_CAUSAL if causal else 0) | (MLA_FLAG_OUT_FP32 if out_fp32 else 0) | (
+        MLA_FLAG_VALIDATE if validate else 0)
+    mla_decode_plan(cache_lens, B, s_q, topk, U, workspace.buf, workspace.nbytes, stream)
+    mla_decode(q, kv_cache, kv_cache.shape[0], block_table, block_table.stride(0), cache_lens, B, s_q,
+               NUM_HEADS, softmax_scale, topk_idx, topk, flags, U, workspace.buf, workspace.nbytes, out,
+               lse, stream)
+    mla_combine(workspace.buf, workspace.nbytes, B, s_q, NUM_HEADS, flags, U, out, lse, stream)
+    return out, lse
+
+
+def decode_step_host(q, kv_cache, block_table, cache_lens, softmax_scale: float, *, device="cuda",
+                     causal: bool = False, topk_idx=None, out_fp32: bool = False, num_units: int = 0,
+                     workspace: Workspace | None = None, dev_buffers=None, out_host=None, lse_host=None):
+    """decode_step for HOST tensors (pinned for speed): H2D copies, the step,
+    D2H copies of O and LSE.  `dev_buffers` may hold preallocated device
+    tensors with the same keys as the inputs to avoid allocation per call."""
+    import torch
+    d = dev_buffers or {}
+
+    def up(name, t):
+        if t is None:
+            return None
+        dst = d.get(name)
+        if dst is None:
+            dst = torch.empty(t.shape, dtype=t.dtype, device=device)
+        dst.copy_(t, non_blocking=True)
+        return dst
+
+    o, l = decode_step(up("q", q), up("kv_cache", kv_cache), up("block_table", block_table),
+                       up("cache_lens", cache_lens), softmax_scale, causal=causal,
+                       topk_idx=up("topk_idx", topk_idx), out_fp32=out_fp32, num_units=num_units,
+                       workspace=workspace, out=d.get("out"), lse=d.get("lse"))
+    if out_host is None:
+        out_host = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+    if lse_host is None:
+        lse_host = torch.empty(l.shape, dtype=l.dtype, pin_memory=True)
+    out_host.copy_(o, non_blocking=True)
+    lse_host.copy_(l, non_blocking=True)
+    torch.cuda.current_stream(device).synchronize()
+    return out_host, lse_host

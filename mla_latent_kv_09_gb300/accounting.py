@@ -1,0 +1,56 @@
+"""Algorithmic work of one MLA decode step (what the roofline is taken on).
+
+FLOPs follow the absorbed-MLA count of "DeepSeek V3/R1 Inference Efficiency
+(2)", §2.4.1 (Compute, "MLA/MQA attention"): Q^T@K = 2*bs*s'*n_head*(c+r)
+and P@V = 2*bs*s'*n_head*c, i.e. 2*128*576 + 2*128*512 = 278,528 flops per
+(query token, visible cache token).
+
+Bytes are the minimum traffic: every visible latent row (576 bf16 = 1152 B)
+read once per request (both MTP tokens share it), plus per (request, query
+token) the 128x576 bf16 query block, the 128x512 output block and the 128
+fp32 LSE values, plus 4 B per block-table entry, top-k index and length
+read.  Partial results of split requests, L2 re-reads and duplicated work
+are implementation overhead and are not counted.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+H, D_QK, D_V, PAGE = 128, 576, 512, 64
+FLOPS_PER_QT = 2 * H * D_QK + 2 * H * D_V  # 278,528
+ROW_BYTES = D_QK * 2
+
+
+def visible_counts(cache_lens, s_q: int, causal: bool, topk_idx=None) -> np.ndarray:
+    """[B, s_q] number of cache positions each query token attends to."""
+    lens = np.maximum(np.asarray(cache_lens, dtype=np.int64), 0)
+    if topk_idx is not None:
+        idx = np.asarray(topk_idx)
+        return ((idx >= 0) & (idx < lens[:, None, None])).sum(axis=-1)
+    t = np.arange(s_q)[None, :]
+    n = lens[:, None] - s_q + t + 1 if causal else np.broadcast_to(lens[:, None], (lens.size, s_q))
+    return np.maximum(n, 0)
+
+
+def step_flops(cache_lens, s_q: int, causal: bool, topk_idx=None) -> int:
+    return int(visible_counts(cache_lens, s_q, causal, topk_idx).sum()) * FLOPS_PER_QT
+
+
+def step_bytes(cache_lens, s_q: int, causal: bool, topk_idx=None, out_bytes_per_elem: int = 2) -> int:
+    lens = np.maximum(np.asarray(cache_lens, dtype=np.int64), 0)
+    B = lens.size
+    if topk_idx is not None:
+        idx = np.asarray(topk_idx)
+        rows = 0
+        for b in range(B):
+            v = idx[b].reshape(-1)
+            rows += np.unique(v[(v >= 0) & (v < lens[b])]).size
+        table = rows  # one block-table entry looked up per gathered row
+        extra = idx.size * 4
+    else:
+        rows = int(lens.sum())
+        table = int(((lens + PAGE - 1) // PAGE).sum())
+        extra = 0
+    per_qt = H * D_QK * 2 + H * D_V * out_bytes_per_elem + H * 4
+    return int(rows * ROW_BYTES + B * s_q * per_qt + 4 * table + extra + 4 * B)

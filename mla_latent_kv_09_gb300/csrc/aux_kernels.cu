@@ -1,0 +1,193 @@
+// aux_kernels.cu — the split-KV planner, the LSE combine and the input
+// validator of the MLA decode library (sm_103a).
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "common.cuh"
+#include "plan.cuh"
+
+namespace mla {
+
+// ------------------------------------------------------------------ plan
+// Block-wide inclusive scan of one int per thread (1024 threads).
+__device__ int block_inclusive_scan(int v, int* s_warp, int& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += n;
+  }
+  if (lane == 31) s_warp[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < (blockDim.x >> 5) ? s_warp[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += n;
+    }
+    s_warp[lane] = w;  // inclusive per-warp totals
+  }
+  __syncthreads();
+  const int res = v + (warp > 0 ? s_warp[warp - 1] : 0);
+  total = s_warp[(blockDim.x >> 5) - 1];
+  __syncthreads();
+  return res;
+}
+
+// One CTA of 1024 threads.  Step 1: tiles and cost prefix per request.
+// Step 2: split count and first partial slot per request.  Step 3: the
+// (request, tile) range of every unit.  Also resets the status word.
+__global__ void __launch_bounds__(1024) mla_plan_kernel(const int* __restrict__ lens, int B, int topk,
+                                                        int U, int* hdr, int* unit_meta, int* req_meta,
+                                                        int slots_cap) {
+  __shared__ int s_warp[32];
+  int carry = 0, tot = 0;
+  for (int base = 0; base < B; base += blockDim.x) {
+    const int b = base + threadIdx.x;
+    const int n = b < B ? plan_tiles(max(lens[b], 0), topk) : 0;
+    const int c = plan_cost(n);
+    const int incl = block_inclusive_scan(c, s_warp, tot);
+    if (b < B) {
+      req_meta[4 * b + 0] = n;
+      req_meta[4 * b + 3] = carry + incl - c;
+    }
+    carry += tot;
+  }
+  const int total = carry;
+  const int W = plan_width(total, U);
+  __syncthreads();
+  carry = 0;
+  for (int base = 0; base < B; base += blockDim.x) {
+    const int b = base + threadIdx.x;
+    int ns = 0;
+    if (b < B) ns = plan_n_splits(req_meta[4 * b + 3], req_meta[4 * b + 0], W, U);
+    const int need = ns > 1 ? ns : 0;
+    const int incl = block_inclusive_scan(need, s_warp, tot);
+    if (b < B) {
+      req_meta[4 * b + 1] = ns;
+      req_meta[4 * b + 2] = carry + incl - need;
+    }
+    carry += tot;
+  }
+  __syncthreads();
+  auto prefix = [&](int b) { return req_meta[4 * b + 3]; };
+  for (int u = threadIdx.x; u < U; u += blockDim.x) {
+    const UnitInfo ui = plan_unit(u, W, total, B, prefix);
+    int* m = unit_meta + 5 * u;
+    m[0] = ui.begin_req; m[1] = ui.begin_tile; m[2] = ui.end_req; m[3] = ui.end_tile;
+    m[4] = ui.first_split;
+  }
+  if (threadIdx.x == 0) {
+    hdr[kHdrStatus] = carry > slots_cap ? static_cast<int>(kStWorkspace) : 0;
+    hdr[kHdrUnits] = U;
+    hdr[kHdrWidth] = W;
+    hdr[kHdrTotal] = total;
+    hdr[kHdrSlots] = carry;
+  }
+}
+
+// ------------------------------------------------------------------ combine
+// Grid (B * s_q, 128 / 8); warp w of a block merges head blockIdx.y * 8 + w.
+// Requests with one split were finished by the decode kernel; requests with
+// no tiles get O = 0, LSE = -inf.
+__global__ void __launch_bounds__(256) mla_combine_kernel(const int* __restrict__ req_meta,
+                                                          const float* __restrict__ part_lse,
+                                                          const float* __restrict__ part_o, int s_q,
+                                                          int out_fp32, void* out, float* lse) {
+  const int bt = blockIdx.x;
+  const int b = bt / s_q, t = bt - b * s_q;
+  const int ns = req_meta[4 * b + 1];
+  if (ns == 1) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.y * 8 + warp;
+  const long long orow = (static_cast<long long>(bt) * kHeads + h) * kDv;
+  float acc[16];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) acc[k] = 0.f;
+  float LSE = -INFINITY;
+  if (ns > 1) {
+    const int slot0 = req_meta[4 * b + 2];
+    float m = -INFINITY;
+    for (int s = lane; s < ns; s += 32)
+      m = fmaxf(m, part_lse[(static_cast<long long>(slot0 + s) * s_q + t) * kHeads + h]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (m != -INFINITY) {
+      float sum = 0.f;
+      for (int s = lane; s < ns; s += 32)
+        sum += expf(part_lse[(static_cast<long long>(slot0 + s) * s_q + t) * kHeads + h] - m);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+      LSE = m + logf(sum);
+      for (int s = 0; s < ns; ++s) {
+        const long long prow = (static_cast<long long>(slot0 + s) * s_q + t) * kHeads + h;
+        const float w = expf(part_lse[prow] - LSE);
+        if (w == 0.f) continue;
+        const float4* src = reinterpret_cast<const float4*>(part_o + prow * kDv) + lane;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float4 v = src[32 * k];
+          acc[4 * k + 0] += w * v.x; acc[4 * k + 1] += w * v.y;
+          acc[4 * k + 2] += w * v.z; acc[4 * k + 3] += w * v.w;
+        }
+      }
+    }
+  }
+  // lane covers dims {4*lane + 128*k .. +3}, k = 0..3 (coalesced 16-byte pieces)
+  if (out_fp32) {
+    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out) + orow) + lane;
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      dst[32 * k] = make_float4(acc[4 * k], acc[4 * k + 1], acc[4 * k + 2], acc[4 * k + 3]);
+  } else {
+    uint2* dst = reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + orow) + lane;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      uint32_t lo, hi;
+      asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(lo) : "f"(acc[4 * k + 1]), "f"(acc[4 * k]));
+      asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(hi) : "f"(acc[4 * k + 3]), "f"(acc[4 * k + 2]));
+      dst[32 * k] = make_uint2(lo, hi);
+    }
+  }
+  if (lane == 0) lse[static_cast<long long>(bt) * kHeads + h] = LSE;
+}
+
+// ------------------------------------------------------------------ validate
+// Checks lengths, the block-table entries the step will read and the top-k
+// indices; records the first problem found in the status word.
+__global__ void mla_validate_kernel(const int* __restrict__ lens, const int* __restrict__ bt,
+                                    long long bt_stride, long long num_pages, int B, int s_q,
+                                    const int* __restrict__ topk_idx, int topk, int* status) {
+  for (int b = blockIdx.x; b < B; b += gridDim.x) {
+    const int L = lens[b];
+    const int* row = bt + static_cast<long long>(b) * bt_stride;
+    if (L < 0) { atomicCAS(status, 0, static_cast<int>(kStBadTable)); continue; }
+    if (topk_idx == nullptr) {
+      if (static_cast<long long>(L) > bt_stride * kPage) {
+        atomicCAS(status, 0, static_cast<int>(kStBadTable));
+        continue;
+      }
+      const int np = (L + kPage - 1) / kPage;
+      for (int j = threadIdx.x; j < np; j += blockDim.x) {
+        const int pg = row[j];
+        if (pg < 0 || pg >= num_pages) atomicCAS(status, 0, static_cast<int>(kStBadTable));
+      }
+    } else {
+      const int* ix = topk_idx + static_cast<long long>(b) * s_q * topk;
+      for (int k = threadIdx.x; k < s_q * topk; k += blockDim.x) {
+        const int v = ix[k];
+        if (v < -1 || v >= L) {
+          atomicCAS(status, 0, static_cast<int>(kStBadIndex));
+        } else if (v >= 0) {
+          const long long pi = v / kPage;
+          if (pi >= bt_stride || row[pi] < 0 || row[pi] >= num_pages)
+            atomicCAS(status, 0, static_cast<int>(kStBadTable));
+        }
+      }
+    }
+  }
+}
+
+}  // namespace mla

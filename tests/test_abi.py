@@ -1,0 +1,93 @@
+"""The C-ABI library builds for sm_103a, loads, and exports every declared
+entry point; host-side argument checks answer without touching a GPU."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import mla_latent_kv_09_gb300 as m
+from mla_latent_kv_09_gb300 import build as mbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mla_decode.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(mla_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    mbuild.build()
+    return m.load()
+
+
+def test_header_declares_the_three_calls_and_helpers():
+    names = declared_functions()
+    for n in ["mla_decode_plan", "mla_decode", "mla_combine", "mla_decode_workspace_size",
+              "mla_status_string", "mla_default_num_units", "mla_decode_plan_host",
+              "mla_workspace_status"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert name in m.SIGNATURES, name
+
+
+def test_status_strings(lib):
+    for code in range(0, 9):
+        s = m.mla_status_string(code)
+        assert s.startswith("MLA_")
+    assert m.mla_status_string(99) == "unknown mla_status"
+
+
+def test_workspace_size_is_pure_host_arithmetic(lib):
+    n = m.mla_decode_workspace_size(64, 2, 128, 38)
+    slots = 2 * 38
+    assert n >= slots * 2 * 128 * 512 * 4 + 64 * 16
+    with pytest.raises(m.MlaError):
+        m.mla_decode_workspace_size(64, 2, 64, 38)  # 64 heads: unsupported
+    with pytest.raises(m.MlaError):
+        m.mla_decode_workspace_size(0, 1, 128, 10)
+
+
+def test_null_pointers_and_bad_shapes_are_rejected_before_any_launch(lib):
+    # every argument check below happens on the host, before the device is touched
+    f = lib.mla_decode
+    ok_ptr = 1 << 20
+    args = [ok_ptr, ok_ptr, 10, ok_ptr, 4, ok_ptr, 2, 1, 128, 0.07, None, 0, 0, 8, ok_ptr, 1 << 30,
+            ok_ptr, ok_ptr, None]
+    a = list(args); a[0] = None
+    assert f(*a) == m.MLA_ERR_INVALID_ARG
+    a = list(args); a[8] = 64
+    assert f(*a) == m.MLA_ERR_UNSUPPORTED
+    a = list(args); a[7] = 3
+    assert f(*a) == m.MLA_ERR_UNSUPPORTED
+    a = list(args); a[0] = ok_ptr + 8  # q not 16-byte aligned
+    assert f(*a) == m.MLA_ERR_INVALID_ARG
+    a = list(args); a[10] = ok_ptr  # index list without a length
+    assert f(*a) == m.MLA_ERR_INVALID_ARG
+    a = list(args); a[12] = 1 << 7  # unknown flag
+    assert f(*a) == m.MLA_ERR_INVALID_ARG
+    a = list(args); a[9] = float("nan")
+    assert f(*a) == m.MLA_ERR_INVALID_ARG
+    assert lib.mla_combine(None, 0, 1, 1, 128, 0, 1, ok_ptr, ok_ptr, None) == m.MLA_ERR_INVALID_ARG
+    assert lib.mla_decode_plan(None, 1, 1, 0, 1, ok_ptr, 1 << 20, None) == m.MLA_ERR_INVALID_ARG
+
+
+def test_python_binding_raises_when_library_missing(tmp_path):
+    from mla_latent_kv_09_gb300 import _binding
+    saved = _binding._lib
+    try:
+        _binding._lib = None
+        with pytest.raises(RuntimeError):
+            _binding.load(str(tmp_path / "nope.so"))
+    finally:
+        _binding._lib = saved

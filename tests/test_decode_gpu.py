@@ -1,0 +1,216 @@
+"""Parity of the CUDA decode path against the fp64 oracle (GPU required).
+
+Tolerances (the stated acceptance bar for this operation): O max-abs <= 2e-2,
+O mean-abs <= 2e-3, LSE abs <= 1e-3.  Reading of the "fp32-accumulated bf16"
+output: the bar is checked on the fp32 O the kernels produce before the final
+cast (MLA_FLAG_OUT_FP32 - same kernels, only the store differs) for every
+workload; the production bf16 O is also checked, against the plain bar where
+|O| is small, and where rows scaled x8 make |O| reach ~30 (long_b128), against
+2e-2 + 2^-8 * |O_ref| (the bf16 half-ulp at that magnitude plus the bar).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import mla_latent_kv_09_gb300 as m
+import oracle
+import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+O_MAX, O_MEAN, LSE_MAX = 2e-2, 2e-3, 1e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _build():
+    from mla_latent_kv_09_gb300 import build
+    build.build()
+    m.load()
+    assert torch.cuda.is_available()
+
+
+def run(w, out_fp32=True, num_units=0, validate=False, q=None, kv=None, table=None, topk_idx="same"):
+    o, lse = m.decode_step(w.q if q is None else q, w.kv if kv is None else kv,
+                           w.block_table if table is None else table, w.cache_lens, w.softmax_scale,
+                           causal=w.causal, topk_idx=w.topk_idx if topk_idx == "same" else topk_idx,
+                           out_fp32=out_fp32, num_units=num_units, validate=validate)
+    torch.cuda.synchronize()
+    return o.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64)
+
+
+def reference(w, select=None):
+    h = wl.host_arrays(w)
+    return oracle.mla_decode(h["q_bits"], h["kv_bits"], h["block_table"], h["cache_lens"],
+                             h["softmax_scale"], causal=h["causal"], topk_idx=h["topk_idx"],
+                             select=select)
+
+
+def assert_close(o, lse, o_ref, lse_ref, select=None, bf16_scaled=False):
+    if select is not None:
+        idx = tuple(np.array(select).T)
+        o, lse, o_ref, lse_ref = o[idx], lse[idx], o_ref[idx], lse_ref[idx]
+    fin = np.isfinite(lse_ref)
+    assert np.array_equal(np.isfinite(lse), fin), "empty rows must give LSE = -inf exactly"
+    assert np.all(o[~fin] == 0), "empty rows must give O = 0"
+    err = np.abs(o - o_ref)
+    if bf16_scaled:
+        assert np.all(err <= O_MAX + 2.0 ** -8 * np.abs(o_ref)), err.max()
+    else:
+        assert err.max() <= O_MAX, f"O max-abs {err.max():.3e}"
+        assert err.mean() <= O_MEAN, f"O mean-abs {err.mean():.3e}"
+    if fin.any():
+        le = np.abs(lse[fin] - lse_ref[fin]).max()
+        assert le <= LSE_MAX, f"LSE max-abs {le:.3e}"
+
+
+# ---------------------------------------------------------------- workloads, small sizes (full compare)
+
+SMALL = [
+    ("single", {}),
+    ("uniform_b32", dict(batch=4, length=1000)),
+    ("mtp_b64", dict(batch=8, length=1000)),
+    ("long_b128", dict(batch=3, length=3000)),
+    ("sparse_b80", dict(batch=4, length=5000)),
+]
+
+
+@pytest.mark.parametrize("name,kw", SMALL, ids=[s[0] for s in SMALL])
+def test_small_workloads_fp32_and_bf16(name, kw):
+    w = wl.make_config(name, device="cuda", **kw)
+    o_ref, lse_ref = reference(w)
+    o, lse = run(w, out_fp32=True)
+    assert_close(o, lse, o_ref, lse_ref)
+    ob, lseb = run(w, out_fp32=False)
+    assert_close(ob, lseb, o_ref, lse_ref, bf16_scaled=(name == "long_b128"))
+    assert np.array_equal(lse, lseb)
+
+
+# ---------------------------------------------------------------- full sizes, sampled rows
+
+FULL = [("uniform_b32", 6), ("mtp_b64", 8), ("long_b128", 3), ("sparse_b80", 4)]
+
+
+@pytest.mark.parametrize("name,nsample", FULL, ids=[f[0] for f in FULL])
+def test_full_size_workloads_sampled(name, nsample):
+    w = wl.make_config(name, device="cuda")
+    rng = np.random.default_rng(5)
+    bs = sorted(rng.choice(w.batch, nsample, replace=False).tolist())
+    sel = [(b, t) for b in bs for t in range(w.s_q)]
+    o, lse = run(w, out_fp32=True)
+    o_ref, lse_ref = reference(w, select=sel)
+    assert_close(o, lse, o_ref, lse_ref, select=sel)
+    ob, lseb = run(w, out_fp32=False)
+    assert_close(ob, lseb, o_ref, lse_ref, select=sel, bf16_scaled=(name == "long_b128"))
+
+
+# ---------------------------------------------------------------- edge cases
+
+@pytest.mark.parametrize("L", [1, 2, 63, 64, 65, 127, 129, 8192])
+def test_lengths_around_tile_edges(L):
+    w = wl.make_workload(f"len{L}", [L, 3 * L + 1], seed=L, device="cuda")
+    o_ref, lse_ref = reference(w)
+    o, lse = run(w)
+    assert_close(o, lse, o_ref, lse_ref)
+
+
+def test_one_request_split_across_many_units_matches_unsplit():
+    w = wl.make_workload("long1", [8192], seed=3, device="cuda")
+    o_ref, lse_ref = reference(w)
+    o_many, lse_many = run(w)  # default: the request is cut across ~22 units
+    o_one, lse_one = run(w, num_units=1)  # one unit: no split, no combine
+    assert_close(o_many, lse_many, o_ref, lse_ref)
+    assert_close(o_one, lse_one, o_ref, lse_ref)
+    assert np.abs(o_many - o_one).max() <= O_MAX
+
+
+def test_causal_two_tokens_with_empty_first_row():
+    # L = 1: token 0 sees nothing (O = 0, LSE = -inf), token 1 sees one row
+    w = wl.make_workload("c", [1, 2, 65, 130], s_q=2, causal=True, seed=9, device="cuda")
+    o_ref, lse_ref = reference(w)
+    o, lse = run(w)
+    assert np.all(np.isneginf(lse[0, 0])) and np.all(o[0, 0] == 0)
+    assert_close(o, lse, o_ref, lse_ref)
+
+
+def test_zero_length_request_gives_empty_result():
+    w = wl.make_workload("z", [0, 100, 0], seed=4, device="cuda")
+    o, lse = run(w)
+    o_ref, lse_ref = reference(w)
+    assert np.all(np.isneginf(lse[0])) and np.all(o[0] == 0) and np.all(np.isneginf(lse[2]))
+    assert_close(o, lse, o_ref, lse_ref)
+
+
+def test_sparse_lists_with_one_entry_and_with_none():
+    w = wl.make_workload("s", [3000, 3000], topk=128, seed=6, device="cuda")
+    idx = w.topk_idx.clone()
+    idx[0, 0, :] = -1
+    idx[0, 0, 77] = 1234  # a single visible row, placed mid-list
+    idx[1, 0, :] = -1  # nothing visible
+    w.topk_idx = idx
+    o_ref, lse_ref = reference(w)
+    o, lse = run(w)
+    assert np.all(np.isneginf(lse[1])) and np.all(o[1] == 0)
+    assert_close(o, lse, o_ref, lse_ref)
+
+
+def test_garbage_past_the_end_of_the_last_page_is_ignored():
+    w = wl.make_workload("g", [70, 10], shuffle=False, seed=8, device="cuda")
+    o_ref, lse_ref = reference(w)
+    kv = w.kv.clone()
+    flat = kv.view(-1, 576)
+    nan = torch.tensor(float("nan"), dtype=torch.bfloat16, device="cuda")
+    flat[70:128] = nan  # rows 70..127 of request 0's pages lie past its length
+    flat[128 + 10:192] = nan
+    o, lse = run(w, kv=kv)
+    assert np.isfinite(o).all()
+    assert_close(o, lse, o_ref, lse_ref)
+
+
+# ---------------------------------------------------------------- invariants
+
+def test_page_permutation_gives_identical_output():
+    w = wl.make_config("uniform_b32", device="cuda", batch=3, length=900)
+    o1, l1 = run(w)
+    perm = torch.randperm(w.num_pages, generator=torch.Generator().manual_seed(1)).cuda()
+    inv = torch.argsort(perm)
+    kv2 = w.kv[perm]
+    t = w.block_table.long()
+    table2 = torch.where(t >= 0, inv[t.clamp(min=0)], t).int()
+    o2, l2 = run(w, kv=kv2, table=table2)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+def test_repeated_calls_are_bit_identical():
+    w = wl.make_config("mtp_b64", device="cuda", batch=16, length=3000)
+    a = run(w)
+    b = run(w)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_sparse_full_index_list_matches_dense():
+    w = wl.make_workload("d", [700, 1000], seed=12, device="cuda")
+    od, ld = run(w)
+    idx = torch.full((2, 1, 1024), -1, dtype=torch.int32)
+    idx[0, 0, :700] = torch.arange(700)
+    idx[1, 0, :1000] = torch.arange(1000)
+    os_, ls = run(w, topk_idx=idx.cuda())
+    assert np.abs(od - os_).max() <= 1e-5 and np.abs(ld - ls).max() <= 1e-5
+
+
+# ---------------------------------------------------------------- validate mode
+
+def test_validate_reports_bad_table_and_bad_index():
+    w = wl.make_workload("v", [200, 300], seed=2, device="cuda")
+    run(w, validate=True)  # clean inputs pass
+    bad = w.block_table.clone()
+    bad[1, 2] = w.num_pages + 5
+    with pytest.raises(m.MlaError) as e:
+        run(w, table=bad, validate=True)
+    assert e.value.status == m.MLA_ERR_BAD_TABLE
+    ws = wl.make_workload("vs", [200, 300], topk=64, seed=2, device="cuda")
+    idx = ws.topk_idx.clone()
+    idx[0, 0, 3] = 250  # beyond request 0's 200 tokens
+    with pytest.raises(m.MlaError) as e:
+        run(ws, topk_idx=idx, validate=True)
+    assert e.value.status == m.MLA_ERR_BAD_INDEX

@@ -1,0 +1,113 @@
+"""Host mirror of the split-KV planner: every (request, tile) is covered
+exactly once, in order, by equally loaded unit ranges, and the split and
+slot bookkeeping the combine step relies on is consistent."""
+
+import numpy as np
+import pytest
+
+import mla_latent_kv_09_gb300 as m
+from mla_latent_kv_09_gb300 import build as mbuild
+
+C0 = 2  # per-split fixed cost in tiles (matches the planner)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    mbuild.build()
+    m.load()
+
+
+def expand(um, rm):
+    """Per unit: list of (request, tile) pairs it processes, in order."""
+    B = rm.shape[0]
+    units = []
+    for bb, bt, eb, et, fs in um:
+        work = []
+        b = bb
+        while b < B and (b < eb or (b == eb and et > 0)):
+            t0 = bt if b == bb else 0
+            t1 = et if b == eb else rm[b, 0]
+            work += [(b, t) for t in range(t0, t1)]
+            b += 1
+        units.append(work)
+    return units
+
+
+def check_plan(lens, U, topk=0):
+    um, rm = m.mla_decode_plan_host(lens, topk, U)
+    lens = np.asarray(lens)
+    ntiles = np.array([(k + 63) // 64 for k in ([topk] * len(lens) if topk else np.maximum(lens, 0))])
+    assert np.array_equal(rm[:, 0], ntiles)
+    units = expand(um, rm)
+    flat = [w for u in units for w in u]
+    want = [(b, t) for b in range(len(lens)) for t in range(ntiles[b])]
+    assert flat == want  # each (request, tile) exactly once, in order
+    # split counts: number of units touching each request
+    touch = np.zeros(len(lens), int)
+    for u in units:
+        for b in sorted({b for b, _ in u}):
+            touch[b] += 1
+    assert np.array_equal(rm[:, 1], touch)
+    # slots: split requests get disjoint consecutive ranges; <= 2U in total
+    used = []
+    for b in range(len(lens)):
+        if rm[b, 1] > 1:
+            used += list(range(rm[b, 2], rm[b, 2] + rm[b, 1]))
+    assert len(used) == len(set(used)) and len(used) <= 2 * U
+    # first_split: the split index of a unit's first segment
+    seen = np.zeros(len(lens), int)
+    for ui, u in enumerate(units):
+        if not u:
+            continue
+        b0 = u[0][0]
+        assert um[ui, 4] == seen[b0]
+        for b in sorted({b for b, _ in u}):
+            seen[b] += 1
+    # balance: unit cost (tiles + C0 per segment) within W + C0 of the mean
+    costs = [len(u) + C0 * len({b for b, _ in u}) for u in units]
+    total = int(sum(n + C0 for n in ntiles if n > 0))
+    W = max(-(-total // U), C0 + 4)
+    assert max(costs) <= W + C0
+    return um, rm, units
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_lengths(seed):
+    rng = np.random.default_rng(seed)
+    B = int(rng.integers(1, 200))
+    lens = rng.integers(0, 9000, B)
+    lens[rng.random(B) < 0.1] = 0
+    U = int(rng.integers(1, 200))
+    check_plan(lens, U)
+
+
+def test_decode_workload_shapes():
+    check_plan([4096] * 32, 74)
+    check_plan(np.random.default_rng(0).integers(1, 8193, 64), 37)
+    check_plan([32768] * 128, 74)
+    check_plan([65536] * 80, 74, topk=2048)
+    check_plan([256], 74)
+
+
+def test_one_long_request_is_split_across_all_units():
+    um, rm, units = check_plan([8192], 64)
+    # 128 tiles + C0, at least C0 + 4 cost per unit -> 22 units
+    assert rm[0, 1] == sum(1 for u in units if u) == -(-130 // (C0 + 4))
+
+
+def test_single_unit_never_splits():
+    um, rm, units = check_plan([100, 5000, 1, 64], 1)
+    assert (rm[:, 1] == 1).all()
+
+
+def test_empty_requests_have_no_work():
+    um, rm, units = check_plan([0, 0, 70, 0], 8)
+    assert rm[0, 1] == 0 and rm[1, 1] == 0 and rm[3, 1] == 0 and rm[2, 1] >= 1
+
+
+def test_balance_on_uniform_batch_is_tight():
+    um, rm, units = check_plan([4096] * 32, 74)
+    sizes = [len(u) for u in units]
+    # makespan: no unit holds more than W = ceil(total cost / U) tiles
+    assert max(sizes) <= -(-(32 * (64 + C0)) // 74)
+    assert sum(1 for x in sizes if x) >= 72
