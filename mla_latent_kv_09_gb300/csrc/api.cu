@@ -26,7 +26,7 @@ int decode_threads();
 cudaError_t decode_set_attrs();
 cudaError_t decode_max_clusters(int* n, int num_clusters_hint);
 cudaError_t decode_launch(bool sparse, int num_clusters, cudaStream_t stream, const DecodeParams& p,
-                          const CUtensorMap& tm_q, const CUtensorMap& tm_kv);
+                          const CUtensorMap& tm_kv);
 }  // namespace mla
 
 using namespace mla;
@@ -264,11 +264,10 @@ int mla_decode(const void* q, const void* kv_cache, int64_t num_pages, const int
   p.part_lse = reinterpret_cast<float*>(ws + L.part_lse);
   p.part_o = reinterpret_cast<float*>(ws + L.part_o);
 
-  CUtensorMap tm_q, tm_kv;
-  if ((rc = encode_2d(&tm_q, q, static_cast<uint64_t>(batch) * s_q * kHeads, kHeads)) != MLA_OK) return rc;
+  CUtensorMap tm_kv;
   if ((rc = encode_2d(&tm_kv, kv_cache, static_cast<uint64_t>(num_pages) * kPage, kPage)) != MLA_OK) return rc;
 
-  const cudaError_t e = decode_launch(topk_idx != nullptr, U * s_q, s, p, tm_q, tm_kv);
+  const cudaError_t e = decode_launch(topk_idx != nullptr, U * s_q, s, p, tm_kv);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return MLA_ERR_CUDA;

@@ -6,27 +6,34 @@
 // contract all 576 dims, values are the first 512 dims of the same row.
 // Cached rows sit in 64-token pages reached through a block table.
 //
-// How (one work unit = one 2-CTA cluster on a pair of SMs):
-//   * O = 128 heads x 512 fp32 fills a whole SM's tensor memory, so the pair
-//     splits the row: CTA 0 owns latent dims [0, 256) and O columns [0, 256),
-//     CTA 1 owns dims [256, 576) (latent 256..511 + RoPE) and O columns
-//     [256, 512).  Each cache byte is fetched from HBM exactly once.
-//   * Per 64-token tile: each CTA computes its partial scores
-//     S_r = Q[:, dims_r] K[:, dims_r]^T on tcgen05 (M=128, N=64, K=256/320,
-//     fp32 in TMEM), the two partials are swapped through distributed shared
-//     memory and added (fp32 addition commutes, so both CTAs hold bit-equal
-//     scores and take identical softmax decisions), the online softmax runs
-//     in fp32 (exp2 domain, running max with a lazy-rescale threshold), P goes
-//     to shared memory as bf16 and each CTA accumulates O_r += P V_r on
-//     tcgen05 (M=128, N=256, K=64) with V_r read from the same smem tile.
-//   * A persistent grid: each unit walks a contiguous range of (request,
-//     tile) work from the plan; a request cut by a range boundary writes a
-//     normalised fp32 partial plus its LSE, merged later by the combine
-//     kernel (the split-K remedy of "The 31-Millisecond Smoking Gun").
+// One work unit = one 2-CTA cluster on a pair of SMs.  The fp32 output
+// O = 128 heads x 512 fills one SM's whole tensor memory, so the pair splits
+// the work by stage of the attention rather than by dimension:
 //
-// Warp roles (288 threads): warps 0-3 softmax / epilogue (thread i owns head
-// row i = TMEM lane i), warp 4 issues MMAs and owns TMEM, warps 5-8 load
-// (dense: one thread drives TMA; sparse: 128 threads gather rows).
+//   CTA 0, "S side": Q (128 x 576 bf16) lives in tensor memory as the A
+//     operand; per 64-token tile it computes S = Q K^T on tcgen05 (M=128,
+//     N=64, K=576, fp32 in TMEM), runs the online softmax in fp32 (exp2
+//     domain, lazy rescale: the reference max moves only when a score beats
+//     it by more than 2^8) and streams the fp16 weights P plus a per-row
+//     rescale factor into CTA 1's shared memory with st.async, which
+//     completes on CTA 1's mbarrier (no round trip, no fence).
+//   CTA 1, "O side": owns O (128 x 512 fp32, all 512 TMEM columns); per tile
+//     it converts the value part of the tile to fp16 in shared memory (scaled
+//     by 2^-8 so the fp16 range covers |v| < 2^24), rescales O rows when the
+//     S side moved the max, and accumulates O += P V on tcgen05 (M=128,
+//     N=2x256, K=64).  P and V in fp16 keep 11 significant bits on the
+//     softmax weights (bf16 would keep 8), which is what holds the O error
+//     under 2e-2 when a few rows dominate the softmax.
+//
+// Both CTAs fetch the tile with TMA (the O side only the 512 value dims);
+// the second fetch of the pair is served by L2.  A persistent grid walks the
+// split-KV plan: a request cut by a unit boundary writes a normalised fp32
+// partial plus its LSE, merged by the combine kernel (the split-K remedy of
+// "The 31-Millisecond Smoking Gun").
+//
+// Warps (320 threads): 0-3 softmax (S side) / O correction + epilogue (O
+// side), thread i = head row i = TMEM lane i; 4 MMA issue + TMEM owner;
+// 5 TMA producer; 6-9 sparse row gather (S side) / V conversion (O side).
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -35,43 +42,61 @@
 
 namespace mla {
 
-constexpr int kQChunkBytes = kHeads * 128;   // 128 rows x 64 bf16
-constexpr int kKvChunkBytes = kPage * 128;   // 64 rows x 64 bf16
-constexpr int kNqMax = 5;
-constexpr int kStages = 2;
-constexpr int kQBytes = kNqMax * kQChunkBytes;       // 81920
-constexpr int kStageBytes = kNqMax * kKvChunkBytes;  // 40960
-constexpr int kPBytes = kHeads * 128;                // 128 rows x 64 bf16
-constexpr int kXBytes = kHeads * 64 * 4;             // 128 rows x 64 fp32
+constexpr int kChunkBytes = kPage * 128;         // 64 rows x 64 bf16, 128B-swizzled
+constexpr int kStages = 3;
+constexpr int kStageS = kNumChunks * kChunkBytes;  // 9 chunks: all 576 dims
+constexpr int kStageO = 8 * kChunkBytes;           // 8 chunks: the 512 value dims
+constexpr int kPBytes = kHeads * 128;              // 128 rows x 64 fp16
 
-constexpr int kOffQ = 0;
-constexpr int kOffKv = kOffQ + kQBytes;
-constexpr int kOffP = kOffKv + kStages * kStageBytes;
-constexpr int kOffX = kOffP + 2 * kPBytes;
-constexpr int kOffBar = kOffX + kXBytes;
+// Shared-memory layout (offsets from a 1024-aligned base).  The barrier block
+// sits at the same offset in both CTAs (multicast commits rely on it).
+constexpr int kOffStage = 0;
+constexpr int kOffP = kStages * kStageO;             // O side: 196608
+constexpr int kOffAlpha = kOffP + 2 * kPBytes;       // O side: float[2][128]
+constexpr int kOffFin = kOffAlpha + 2 * kHeads * 4;  // O side: float[2][128]
+constexpr int kOffBar = kOffFin + 2 * kHeads * 4;    // 231424
 constexpr int kBarBytes = 256;
-constexpr int kOffMask = kOffBar + kBarBytes;  // sparse: 64-bit row-valid mask per stage
-constexpr int kMaskBytes = 16;
-constexpr int kSmemBytes = kOffMask + kMaskBytes + 1024;  // + alignment slack
+constexpr int kSmemUsed = kOffBar + kBarBytes;
+constexpr int kAlignSlack = 768;
+constexpr int kSmemBytes = kSmemUsed + kAlignSlack;  // 232448 = the opt-in maximum
+static_assert(kStages * kStageS <= kOffBar, "S-side stages overlap the barrier block");
 
+// Tensor-memory columns.
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColO = 0;
-constexpr uint32_t kColS = 256;  // two 64-column score buffers
+constexpr uint32_t kColS = 0;     // S side: two 64-column score buffers
+constexpr uint32_t kColQ = 128;   // S side: Q, 288 columns (576 bf16 packed in pairs)
+constexpr uint32_t kColO = 0;     // O side: O, 512 columns
 
-constexpr int kNumThreads = 288;
-constexpr float kRescaleLog2 = 8.0f;  // rescale O only when the max grows by > 2^8
+constexpr int kNumThreads = 320;
+constexpr float kRescaleLog2 = 8.0f;
+constexpr float kVScale = 0.00390625f;  // 2^-8 applied to V in fp16; undone at the end
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 constexpr uint64_t kDrainNs = 20000000ull;
 
 enum Bar {
-  kKvFull0, kKvFull1, kKvEmpty0, kKvEmpty1, kQFull, kQEmpty, kSFull0, kSFull1, kSFree0,
-  kSFree1, kPFull0, kPFull1, kPFree0, kPFree1, kOFull, kOFree, kXFull, kXFree, kMmaDone,
-  kNumBars
+  kKF = 0,        // [3] tile landed (TMA tx, or 128 gather arrivals)
+  kKE = 3,        // [3] tile free (MMA commit)
+  kVR = 6,        // [3] O side: fp16 V ready (128 arrivals)
+  kQR = 9,        // S side: Q in TMEM (128 arrivals)
+  kQF = 10,       // S side: Q free (commit after a segment's last QK)
+  kSF = 11,       // [2] S side: scores ready (commit)
+  kSE = 13,       // [2] S side: scores read (128 arrivals)
+  kPFree = 15,    // [2] S side: O side finished PV on that P slot (remote commit)
+  kPM = 17,       // [2] O side: P message landed (1 arrival + tx bytes)
+  kPR = 19,       // [2] O side: O corrected, PV may go (128 arrivals)
+  kPD = 21,       // O side: a PV finished (commit)
+  kOF = 22,       // O side: segment's last PV finished (commit)
+  kOE = 23,       // O side: epilogue read O (128 arrivals)
+  kMmaDone = 24,  // teardown
+  kNumBars = 25
 };
-static_assert(kNumBars * 8 + 16 <= kBarBytes, "barrier area");
+static_assert(kNumBars * 8 + 16 <= kBarBytes, "barrier block");
 
+// kind::f16 instruction descriptors: S = Q K^T with bf16 operands; O += P V
+// with fp16 operands (A and B of one MMA always share a type).
 constexpr uint32_t kIdescQK = idesc_bf16(128, 64, 0);
-constexpr uint32_t kIdescPV = idesc_bf16(128, 256, 1);
+constexpr uint32_t kIdescPV = (1u << 4) | (0u << 7) | (0u << 10) | (1u << 16) | ((256u >> 3) << 17) |
+                              ((128u >> 4) << 24);
 
 struct Seg {
   int b, t0, t1, n_tiles, slot;  // slot < 0: write the final output
@@ -103,6 +128,14 @@ struct SegIter {
       if (t0 < t1) return true;
     }
     return false;
+  }
+};
+
+// Position in the 3-deep tile ring.
+struct Ring3 {
+  uint32_t idx = 0, phase = 0;
+  __device__ void advance() {
+    if (++idx == kStages) { idx = 0; phase ^= 1u; }
   }
 };
 
@@ -142,13 +175,71 @@ __device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity) {
   }
 }
 
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const Ctl& c) {
+  return __all_sync(0xffffffffu, wait_bar<false>(bar, parity, c));
+}
+
+// tcgen05.mma with the A operand in tensor memory.
+__device__ __forceinline__ void umma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}"
+      ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+}
+
+// Commit that arrives on the mbarrier at the same offset in every CTA of `mask`.
+__device__ __forceinline__ void umma_commit_multicast(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar), "h"(mask) : "memory");
+}
+
+// Remote shared-memory stores that complete on the destination CTA's mbarrier.
+__device__ __forceinline__ void st_async_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                                            uint32_t bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];"
+      ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d), "r"(bar) : "memory");
+}
+__device__ __forceinline__ void st_async_b32(uint32_t addr, uint32_t v, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];"
+               ::"r"(addr), "r"(v), "r"(bar) : "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ float f16_lo(uint32_t v) {
+  float f;
+  asm("{\n .reg .f16 h, x;\n mov.b32 {h, x}, %1;\n cvt.f32.f16 %0, h;\n}" : "=f"(f) : "r"(v));
+  return f;
+}
+__device__ __forceinline__ float f16_hi(uint32_t v) {
+  float f;
+  asm("{\n .reg .f16 h, x;\n mov.b32 {x, h}, %1;\n cvt.f32.f16 %0, h;\n}" : "=f"(f) : "r"(v));
+  return f;
+}
+
+// bf16x2 word -> fp16x2 word of the values times 2^-8.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2_scaled(uint32_t w) {
+  return pack_f16x2(__uint_as_float(w << 16) * kVScale, __uint_as_float(w & 0xffff0000u) * kVScale);
+}
+
+// Bytes of one P message (fp16 P tile, per-row rescale, and at the end of a
+// segment the per-row final scale).
+__host__ __device__ constexpr uint32_t p_message_bytes(bool last) {
+  return static_cast<uint32_t>(kPBytes + kHeads * 4 + (last ? kHeads * 4 : 0));
+}
+
 template <bool kSparse>
 __global__ void __launch_bounds__(kNumThreads, 1)
-mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tm_q,
-                  const __grid_constant__ CUtensorMap tm_kv) {
+mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tm_kv) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t mis = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+  uint8_t* smem = smem_raw + mis;
   const uint32_t sbase = smem_u32(smem);
   const uint32_t rank = cluster_ctarank();
   const uint32_t peer = rank ^ 1u;
@@ -158,41 +249,45 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
   const int cluster_id = blockIdx.x >> 1;
   const int unit = cluster_id % U;
   const int tok = cluster_id / U;
-  const int nq = rank == 0 ? 4 : 5;          // 64-dim chunks this CTA owns
-  const int chunk0 = rank == 0 ? 0 : 4;
+  const bool s_side = rank == 0;
 
   {  // a unit with no work leaves at once (both CTAs see the same range)
     const int* um = p.unit_meta + 5 * unit;
     if (um[0] >= p.batch || (um[0] == um[2] && um[1] >= um[3])) return;
   }
+  if (mis > kAlignSlack) {  // never touch shared memory past the end of the allocation
+    if (threadIdx.x == 0) atomicCAS(p.ws_hdr + kHdrStatus, 0, static_cast<int>(kStWorkspace));
+    return;
+  }
 
-  const uint32_t sQ = sbase + kOffQ;
-  const uint32_t sKv = sbase + kOffKv;
+  const uint32_t sStage = sbase + kOffStage;
   const uint32_t sP = sbase + kOffP;
-  const uint32_t sX = sbase + kOffX;
+  const uint32_t sAlpha = sbase + kOffAlpha;
+  const uint32_t sFin = sbase + kOffFin;
   auto bar = [&](int i) -> uint32_t { return sbase + kOffBar + 8u * static_cast<uint32_t>(i); };
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + kOffBar + 8 * kNumBars);
   // misc[0] = TMEM base address, misc[1] = abort flag
+  const int stage_bytes = s_side ? kStageS : kStageO;
+  const int nchunks = s_side ? kNumChunks : 8;
 
   if (threadIdx.x == 0) {
-    mbar_init(bar(kKvFull0), kSparse ? 128 : 1);
-    mbar_init(bar(kKvFull1), kSparse ? 128 : 1);
-    mbar_init(bar(kKvEmpty0), 1);
-    mbar_init(bar(kKvEmpty1), 1);
-    mbar_init(bar(kQFull), 1);
-    mbar_init(bar(kQEmpty), 1);
-    mbar_init(bar(kSFull0), 1);
-    mbar_init(bar(kSFull1), 1);
-    mbar_init(bar(kSFree0), 128);
-    mbar_init(bar(kSFree1), 128);
-    mbar_init(bar(kPFull0), 128);
-    mbar_init(bar(kPFull1), 128);
-    mbar_init(bar(kPFree0), 1);
-    mbar_init(bar(kPFree1), 1);
-    mbar_init(bar(kOFull), 1);
-    mbar_init(bar(kOFree), 128);
-    mbar_init(bar(kXFull), 128);
-    mbar_init(bar(kXFree), 128);
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(bar(kKF + i), kSparse ? 128 : 1);
+      mbar_init(bar(kKE + i), 1);
+      mbar_init(bar(kVR + i), 128);
+    }
+    mbar_init(bar(kQR), 128);
+    mbar_init(bar(kQF), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(kSF + i), 1);
+      mbar_init(bar(kSE + i), 128);
+      mbar_init(bar(kPFree + i), 1);
+      mbar_init(bar(kPM + i), 1);
+      mbar_init(bar(kPR + i), 128);
+    }
+    mbar_init(bar(kPD), 1);
+    mbar_init(bar(kOF), 1);
+    mbar_init(bar(kOE), 128);
     mbar_init(bar(kMmaDone), 1);
     misc[1] = 0u;
     fence_mbar_init();
@@ -201,13 +296,10 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
     tmem_alloc(smem_u32(&misc[0]), kTmemCols);
     tmem_relinquish();
   }
-  if (warp == 5 && lane == 0 && !kSparse) {
-    tma_prefetch_desc(&tm_q);
-    tma_prefetch_desc(&tm_kv);
-  }
+  if (warp == 5 && lane == 0 && !kSparse) tma_prefetch_desc(&tm_kv);
   tc_fence_before();
   __syncthreads();
-  cluster_sync();  // the peer's barriers exist before any remote arrive
+  cluster_sync();  // the peer's barriers exist before any remote operation
   tc_fence_after();
   const uint32_t tmem = misc[0];
 
@@ -215,16 +307,16 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
   ctl.abort = &misc[1];
   ctl.abort_remote = mapa(smem_u32(&misc[1]), peer);
   ctl.status = p.ws_hdr + kHdrStatus;
+  const float NEG_INF = -__int_as_float(0x7f800000);
 
-  if (warp < 4) {
-    // ===================================================== softmax / epilogue
-    const int row = threadIdx.x;  // head = TMEM lane
+  if (warp < 4 && s_side) {
+    // ================================================= S side: Q load + softmax
+    const int row = threadIdx.x;
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-    const uint32_t x_row = sX + static_cast<uint32_t>(row) * 256u;
-    const uint32_t x_row_remote = mapa(x_row, peer);
-    const uint32_t xfull_remote = mapa(bar(kXFull), peer);
-    const uint32_t xfree_remote = mapa(bar(kXFree), peer);
-    const float NEG_INF = -__int_as_float(0x7f800000);
+    const uint32_t rP = mapa(sP, peer) + static_cast<uint32_t>(row) * 128u;
+    const uint32_t rAlpha = mapa(sAlpha, peer) + static_cast<uint32_t>(row) * 4u;
+    const uint32_t rFin = mapa(sFin, peer) + static_cast<uint32_t>(row) * 4u;
+    const uint32_t rPM = mapa(bar(kPM), peer);
     SegIter it(p, unit);
     Seg sg;
     uint32_t g = 0, nseg = 0;
@@ -232,56 +324,75 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
     while (ok && it.next(sg)) {
       const int L = max(p.cache_lens[sg.b], 0);
       const int vis = p.causal ? L - p.s_q + tok + 1 : L;
-      // z: sum of the bf16-rounded weights (normalises O, whose PV product uses
+      const long long bt_row = static_cast<long long>(sg.b) * p.s_q + tok;
+      // ---- Q row -> TMEM (after the previous segment's score MMAs)
+      if (!(ok = warp_wait(bar(kQF), (nseg & 1u) ^ 1u, ctl))) break;
+      tc_fence_after();
+      {
+        const uint4* qrow = reinterpret_cast<const uint4*>(p.q + (bt_row * kHeads + row) * kDqk);
+#pragma unroll 1
+        for (int cc = 0; cc < kNumChunks; ++cc) {
+          uint32_t r[32];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint4 v = __ldg(qrow + cc * 8 + k);
+            r[4 * k] = v.x; r[4 * k + 1] = v.y; r[4 * k + 2] = v.z; r[4 * k + 3] = v.w;
+          }
+          tmem_st32(tmem + lane_base + kColQ + 32u * cc, r);
+        }
+        tmem_wait_st();
+      }
+      tc_fence_before();
+      mbar_arrive(bar(kQR));
+
+      // z: sum of the fp16-rounded weights (normalises O, whose PV product uses
       // exactly those weights); zx: sum of the unrounded weights (for the LSE)
       float m_used = NEG_INF, z = 0.f, zx = 0.f;
+      const int* idx = kSparse ? p.topk_idx + bt_row * p.topk : nullptr;
       for (int j = sg.t0; j < sg.t1; ++j, ++g) {
         const uint32_t sb = g & 1u, ph = (g >> 1) & 1u;
-        ok = __all_sync(0xffffffffu, wait_bar<false>(bar(kSFull0 + sb), ph, ctl));
-        if (kSparse && ok) ok = __all_sync(0xffffffffu, wait_bar<false>(bar(kKvFull0 + sb), ph, ctl));
-        if (!ok) break;
+        const bool last = (j == sg.t1 - 1);
+        if (!(ok = warp_wait(bar(kSF + sb), ph, ctl))) break;
         tc_fence_after();
         float s[64];
         {
           uint32_t r[32];
           tmem_ld32(tmem + lane_base + kColS + 64u * sb, r);
+          uint32_t r2[32];
+          tmem_ld32(tmem + lane_base + kColS + 64u * sb + 32u, r2);
           tmem_wait_ld();
 #pragma unroll
-          for (int c = 0; c < 32; ++c) s[c] = __uint_as_float(r[c]);
-          tmem_ld32(tmem + lane_base + kColS + 64u * sb + 32u, r);
-          tmem_wait_ld();
-#pragma unroll
-          for (int c = 0; c < 32; ++c) s[32 + c] = __uint_as_float(r[c]);
+          for (int c = 0; c < 32; ++c) {
+            s[c] = __uint_as_float(r[c]);
+            s[32 + c] = __uint_as_float(r2[c]);
+          }
         }
         tc_fence_before();
-        mbar_arrive(bar(kSFree0 + sb));
+        mbar_arrive(bar(kSE + sb));
 
-        // ---- swap partial scores with the peer CTA through DSMEM
-        if (!(ok = __all_sync(0xffffffffu, wait_bar<true>(bar(kXFree), (g & 1u) ^ 1u, ctl)))) break;
-#pragma unroll
-        for (int c = 0; c < 16; ++c)
-          st_cluster_v4(x_row_remote + ((static_cast<uint32_t>(c) ^ (row & 15)) << 4), s[4 * c],
-                        s[4 * c + 1], s[4 * c + 2], s[4 * c + 3]);
-        mbar_arrive_remote(xfull_remote);
-        if (!(ok = __all_sync(0xffffffffu, wait_bar<true>(bar(kXFull), g & 1u, ctl)))) break;
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const float4 v = ld_shared_v4f(x_row + ((static_cast<uint32_t>(c) ^ (row & 15)) << 4));
-          s[4 * c] += v.x; s[4 * c + 1] += v.y; s[4 * c + 2] += v.z; s[4 * c + 3] += v.w;
-        }
-        mbar_arrive_remote(xfree_remote);
-
-        // ---- mask, scale to the exp2 domain, running max
+        // ---- mask, scale to the exp2 domain, tile max
         float mt = NEG_INF;
         if (kSparse) {
-          // rows the loaders actually fetched (index in [0, len), page in the pool)
-          const unsigned long long vmask =
-              *reinterpret_cast<const volatile unsigned long long*>(smem + kOffMask + 8 * sb);
+          const int base = j * 64;
+          const bool vec = ((p.topk & 3) == 0) && ((reinterpret_cast<uintptr_t>(idx) & 15) == 0);
 #pragma unroll
-          for (int c = 0; c < 64; ++c) {
-            const float t = ((vmask >> c) & 1ull) ? s[c] * p.scale_log2 : NEG_INF;
-            s[c] = t;
-            mt = fmaxf(mt, t);
+          for (int c4 = 0; c4 < 16; ++c4) {
+            int iv[4];
+            const int pos = base + 4 * c4;
+            if (vec && pos + 3 < p.topk) {
+              const int4 v = __ldg(reinterpret_cast<const int4*>(idx + pos));
+              iv[0] = v.x; iv[1] = v.y; iv[2] = v.z; iv[3] = v.w;
+            } else {
+#pragma unroll
+              for (int k = 0; k < 4; ++k) iv[k] = pos + k < p.topk ? __ldg(idx + pos + k) : -1;
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const bool valid = iv[k] >= 0 && iv[k] < L;
+              const float t = valid ? s[4 * c4 + k] * p.scale_log2 : NEG_INF;
+              s[4 * c4 + k] = t;
+              mt = fmaxf(mt, t);
+            }
           }
         } else {
           const int nvalid = vis - j * 64;
@@ -293,13 +404,10 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
           }
         }
 
-        // ---- online softmax with a lazy rescale: the reference max m_used
-        // moves only when a score exceeds it by more than 2^8, so P <= 256.
-        bool resc = false;
+        // ---- online softmax with a lazy rescale of the reference max
         float alpha = 1.f;
-        if (mt > m_used + kRescaleLog2 || (m_used == NEG_INF && mt != NEG_INF)) {
+        if (mt > m_used + kRescaleLog2) {
           alpha = (m_used == NEG_INF) ? 0.f : ex2_approx(m_used - mt);
-          resc = (m_used != NEG_INF) && (j != sg.t0);
           m_used = mt;
           z *= alpha;
           zx *= alpha;
@@ -314,24 +422,63 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
           for (int c = 0; c < 32; ++c) {
             const float p0 = ex2_approx(s[2 * c] - m_used);
             const float p1 = ex2_approx(s[2 * c + 1] - m_used);
-            pk[c] = pack_bf16x2(p0, p1);
-            zs += __uint_as_float(pk[c] << 16) + __uint_as_float(pk[c] & 0xffff0000u);
+            pk[c] = pack_f16x2(p0, p1);
+            zs += f16_lo(pk[c]) + f16_hi(pk[c]);
             ze += p0 + p1;
           }
           z += zs;
           zx += ze;
         }
 
-        // ---- rescale O (warp-uniform: tcgen05.ld/st are warp-collective)
-        if (__any_sync(0xffffffffu, resc)) {
-          const uint32_t gp = g - 1u;
-          if (!(ok = __all_sync(0xffffffffu,
-                                wait_bar<false>(bar(kPFree0 + (gp & 1u)), (gp >> 1) & 1u, ctl))))
-            break;
+        // ---- P message to the O side, once it is done with this slot
+        if (!(ok = warp_wait(bar(kPFree + sb), ph ^ 1u, ctl))) break;
+        const uint32_t mbar = rPM + 8u * sb;
+        const uint32_t prow = rP + sb * kPBytes;
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          st_async_v4(prow + ((static_cast<uint32_t>(k) ^ (row & 7)) << 4), pk[4 * k], pk[4 * k + 1],
+                      pk[4 * k + 2], pk[4 * k + 3], mbar);
+        st_async_b32(rAlpha + sb * kHeads * 4u, __float_as_uint(alpha), mbar);
+        if (last) {
+          // O_final = O_acc * 2^8 / z (the 2^8 undoes the scaling of V)
+          const float fin = z > 0.f ? 256.f / z : 0.f;
+          st_async_b32(rFin + sb * kHeads * 4u, __float_as_uint(fin), mbar);
+          const float lse = zx > 0.f ? (m_used + log2f(zx)) * 0.69314718055994531f : NEG_INF;
+          if (sg.slot < 0) {
+            p.lse[bt_row * kHeads + row] = lse;
+          } else if (sg.slot < 2 * U) {  // the plan never uses more than 2 * (U - 1) slots
+            p.part_lse[(static_cast<long long>(sg.slot) * p.s_q + tok) * kHeads + row] = lse;
+          }
+        }
+      }
+      ++nseg;
+    }
+  } else if (warp < 4) {
+    // ================================================= O side: O correction + epilogue
+    const int row = threadIdx.x;
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const volatile float* alpha_s = reinterpret_cast<const volatile float*>(smem + kOffAlpha);
+    const volatile float* fin_s = reinterpret_cast<const volatile float*>(smem + kOffFin);
+    SegIter it(p, unit);
+    Seg sg;
+    uint32_t g = 0, nseg = 0;
+    bool ok = true;
+    while (ok && it.next(sg)) {
+      float fin = 0.f;
+      for (int j = sg.t0; j < sg.t1; ++j, ++g) {
+        const uint32_t pb = g & 1u, ph = (g >> 1) & 1u;
+        const bool last = (j == sg.t1 - 1);
+        if (row == 0) mbar_arrive_expect_tx(bar(kPM + pb), p_message_bytes(last));
+        if (!(ok = __all_sync(0xffffffffu, wait_bar<true>(bar(kPM + pb), ph, ctl)))) break;
+        const float alpha = alpha_s[pb * kHeads + row];
+        if (last) fin = fin_s[pb * kHeads + row];
+        const bool resc = (j != sg.t0) && alpha != 1.f;
+        if (__any_sync(0xffffffffu, resc)) {  // tcgen05.ld/st are warp-collective
+          if (!(ok = warp_wait(bar(kPD), (g - 1u) & 1u, ctl))) break;
           tc_fence_after();
           const float a = resc ? alpha : 1.f;
 #pragma unroll 1
-          for (int cc = 0; cc < 8; ++cc) {
+          for (int cc = 0; cc < 16; ++cc) {
             uint32_t r[32];
             const uint32_t ta = tmem + lane_base + kColO + 32u * cc;
             tmem_ld32(ta, r);
@@ -342,246 +489,217 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
           }
           tmem_wait_st();
         }
-
-        // ---- P -> shared memory (K-major, 128-byte swizzle), after PV(g-2)
-        if (!(ok = __all_sync(0xffffffffu, wait_bar<false>(bar(kPFree0 + sb), ph ^ 1u, ctl)))) break;
-        {
-          const uint32_t prow = sP + sb * kPBytes + static_cast<uint32_t>(row) * 128u;
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            st_shared_v4(prow + ((static_cast<uint32_t>(k) ^ (row & 7)) << 4), pk[4 * k],
-                         pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
-        }
-        // rows past the end of the cache in the request's last page may hold
-        // anything (even NaN); zero their value part so 0 * V stays 0
-        if (!kSparse && j == sg.n_tiles - 1 && L < (j + 1) * 64) {
-          const int r0 = L - j * 64;
-          const int n = (64 - r0) * 32;
-          const uint32_t st = sKv + sb * kStageBytes;
-          for (int e = row; e < n; e += 128) {
-            const int rr = r0 + (e >> 5), c16 = e & 31;
-            st_shared_zero16(st + (c16 >> 3) * kKvChunkBytes + rr * 128 +
-                             (((c16 & 7) ^ (rr & 7)) << 4));
-          }
-        }
-        fence_proxy_async_smem();
+        fence_proxy_async_smem();  // P written by st.async, read next by the tensor core
         tc_fence_before();
-        mbar_arrive(bar(kPFull0 + sb));
+        mbar_arrive(bar(kPR + pb));
 
-        // ---- segment epilogue
-        if (j == sg.t1 - 1) {
-          if (!(ok = __all_sync(0xffffffffu, wait_bar<false>(bar(kOFull), nseg & 1u, ctl)))) break;
+        if (last) {  // ---- segment epilogue: O * fin -> global
+          if (!(ok = warp_wait(bar(kOF), nseg & 1u, ctl))) break;
           tc_fence_after();
-          const float inv = z > 0.f ? 1.f / z : 0.f;
-          const float lse = zx > 0.f ? (m_used + log2f(zx)) * 0.69314718055994531f : NEG_INF;
           const long long bt_row = static_cast<long long>(sg.b) * p.s_q + tok;
-          if (sg.slot < 0) {
-            const long long o_off = (bt_row * kHeads + row) * kDv + rank * kVcolsPerCta;
+          if (sg.slot < 0 && !p.out_fp32) {
+            uint16_t* dst0 = static_cast<uint16_t*>(p.out) + (bt_row * kHeads + row) * kDv;
 #pragma unroll 1
-            for (int cc = 0; cc < 8; ++cc) {
+            for (int cc = 0; cc < 16; ++cc) {
               uint32_t r[32];
               tmem_ld32(tmem + lane_base + kColO + 32u * cc, r);
               tmem_wait_ld();
-              if (p.out_fp32) {
-                float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + o_off + 32 * cc);
+              uint4* dst = reinterpret_cast<uint4*>(dst0 + 32 * cc);
 #pragma unroll
-                for (int k = 0; k < 8; ++k)
-                  dst[k] = make_float4(__uint_as_float(r[4 * k]) * inv, __uint_as_float(r[4 * k + 1]) * inv,
-                                       __uint_as_float(r[4 * k + 2]) * inv, __uint_as_float(r[4 * k + 3]) * inv);
-              } else {
-                uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + o_off + 32 * cc);
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                  dst[k] = make_uint4(
-                      pack_bf16x2(__uint_as_float(r[8 * k + 0]) * inv, __uint_as_float(r[8 * k + 1]) * inv),
-                      pack_bf16x2(__uint_as_float(r[8 * k + 2]) * inv, __uint_as_float(r[8 * k + 3]) * inv),
-                      pack_bf16x2(__uint_as_float(r[8 * k + 4]) * inv, __uint_as_float(r[8 * k + 5]) * inv),
-                      pack_bf16x2(__uint_as_float(r[8 * k + 6]) * inv, __uint_as_float(r[8 * k + 7]) * inv));
-              }
+              for (int k = 0; k < 4; ++k)
+                dst[k] = make_uint4(
+                    pack_bf16x2(__uint_as_float(r[8 * k + 0]) * fin, __uint_as_float(r[8 * k + 1]) * fin),
+                    pack_bf16x2(__uint_as_float(r[8 * k + 2]) * fin, __uint_as_float(r[8 * k + 3]) * fin),
+                    pack_bf16x2(__uint_as_float(r[8 * k + 4]) * fin, __uint_as_float(r[8 * k + 5]) * fin),
+                    pack_bf16x2(__uint_as_float(r[8 * k + 6]) * fin, __uint_as_float(r[8 * k + 7]) * fin));
             }
-            if (rank == 0) p.lse[bt_row * kHeads + row] = lse;
-          } else if (sg.slot < 2 * U) {  // the plan never uses more than 2 * (U - 1) slots
-            const long long prow_id = static_cast<long long>(sg.slot) * p.s_q + tok;
-            float* dst0 = p.part_o + (prow_id * kHeads + row) * kDv + rank * kVcolsPerCta;
+          } else if (sg.slot < 2 * U) {
+            float* dst0 = sg.slot < 0
+                ? static_cast<float*>(p.out) + (bt_row * kHeads + row) * kDv
+                : p.part_o + ((static_cast<long long>(sg.slot) * p.s_q + tok) * kHeads + row) * kDv;
 #pragma unroll 1
-            for (int cc = 0; cc < 8; ++cc) {
+            for (int cc = 0; cc < 16; ++cc) {
               uint32_t r[32];
               tmem_ld32(tmem + lane_base + kColO + 32u * cc, r);
               tmem_wait_ld();
               float4* dst = reinterpret_cast<float4*>(dst0 + 32 * cc);
 #pragma unroll
               for (int k = 0; k < 8; ++k)
-                dst[k] = make_float4(__uint_as_float(r[4 * k]) * inv, __uint_as_float(r[4 * k + 1]) * inv,
-                                     __uint_as_float(r[4 * k + 2]) * inv, __uint_as_float(r[4 * k + 3]) * inv);
+                dst[k] = make_float4(__uint_as_float(r[4 * k]) * fin, __uint_as_float(r[4 * k + 1]) * fin,
+                                     __uint_as_float(r[4 * k + 2]) * fin, __uint_as_float(r[4 * k + 3]) * fin);
             }
-            if (rank == 0) p.part_lse[prow_id * kHeads + row] = lse;
           }
           tc_fence_before();
-          mbar_arrive(bar(kOFree));
+          mbar_arrive(bar(kOE));
         }
       }
       ++nseg;
     }
   } else if (warp == 4) {
-    // ===================================================== MMA issuer
+    // ================================================= MMA issue (one thread)
     if (lane == 0) {
       SegIter it(p, unit);
       Seg sg;
+      Ring3 rs;
       uint32_t g = 0, nseg = 0;
       bool ok = true;
-      auto issue_pv = [&](uint32_t gg, bool first) -> bool {
-        const uint32_t pb = gg & 1u, ph = (gg >> 1) & 1u;
-        if (!wait_bar<false>(bar(kPFull0 + pb), ph, ctl)) return false;
-        if (first && !wait_bar<false>(bar(kOFree), (nseg & 1u) ^ 1u, ctl)) return false;
-        tc_fence_after();
-        const uint32_t stg = sKv + pb * kStageBytes;
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t ad = smem_desc(sP + pb * kPBytes + 32u * kk, 16u, 1024u);
-          const uint64_t bd = smem_desc(stg + 2048u * kk, 8192u, 1024u);  // V, MN-major
-          umma_f16(tmem + kColO, ad, bd, kIdescPV, (first && kk == 0) ? 0u : 1u);
-        }
-        umma_commit(bar(kKvEmpty0 + pb));
-        umma_commit(bar(kPFree0 + pb));
-        return true;
-      };
       while (ok && it.next(sg)) {
-        if (!(ok = wait_bar<false>(bar(kQFull), nseg & 1u, ctl))) break;
-        tc_fence_after();
-        for (int j = sg.t0; j < sg.t1; ++j, ++g) {
-          const uint32_t st = g & 1u, ph = (g >> 1) & 1u;
-          if (!(ok = wait_bar<false>(bar(kKvFull0 + st), ph, ctl))) break;
-          if (!(ok = wait_bar<false>(bar(kSFree0 + st), ph ^ 1u, ctl))) break;
+        if (s_side) {
+          if (!(ok = wait_bar<false>(bar(kQR), nseg & 1u, ctl))) break;
           tc_fence_after();
-          const uint32_t stg = sKv + st * kStageBytes;
-          for (int c = 0; c < nq; ++c) {
+        }
+        for (int j = sg.t0; j < sg.t1; ++j, ++g, rs.advance()) {
+          const uint32_t stg = sStage + rs.idx * stage_bytes;
+          const uint32_t sb = g & 1u, ph = (g >> 1) & 1u;
+          if (s_side) {
+            if (!(ok = wait_bar<false>(bar(kKF + rs.idx), rs.phase, ctl))) break;
+            if (!(ok = wait_bar<false>(bar(kSE + sb), ph ^ 1u, ctl))) break;
+            tc_fence_after();
+            for (int c = 0; c < kNumChunks; ++c) {
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t bd = smem_desc(stg + c * kChunkBytes + 32u * kk, 16u, 1024u);
+                umma_f16_tmem_a(tmem + kColS + 64u * sb, tmem + kColQ + 32u * c + 8u * kk, bd, kIdescQK,
+                                (c | kk) != 0 ? 1u : 0u);
+              }
+            }
+            umma_commit(bar(kSF + sb));
+            umma_commit(bar(kKE + rs.idx));
+            if (j == sg.t1 - 1) umma_commit(bar(kQF));
+          } else {
+            const bool first = (j == sg.t0);
+            if (!(ok = wait_bar<false>(bar(kVR + rs.idx), rs.phase, ctl))) break;
+            if (!(ok = wait_bar<false>(bar(kPR + sb), ph, ctl))) break;
+            if (first && !(ok = wait_bar<false>(bar(kOE), (nseg & 1u) ^ 1u, ctl))) break;
+            tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t ad = smem_desc(sQ + c * kQChunkBytes + 32u * kk, 16u, 1024u);
-              const uint64_t bd = smem_desc(stg + c * kKvChunkBytes + 32u * kk, 16u, 1024u);
-              umma_f16(tmem + kColS + 64u * st, ad, bd, kIdescQK, (c | kk) != 0 ? 1u : 0u);
+              const uint64_t ad = smem_desc(sP + sb * kPBytes + 32u * kk, 16u, 1024u);
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const uint64_t bd = smem_desc(stg + h * 4 * kChunkBytes + 2048u * kk, 8192u, 1024u);
+                umma_f16(tmem + kColO + 256u * h, ad, bd, kIdescPV, (first && kk == 0) ? 0u : 1u);
+              }
             }
+            umma_commit(bar(kKE + rs.idx));
+            umma_commit_multicast(bar(kPFree + sb), 1);  // the S side may reuse this P slot
+            umma_commit(bar(kPD));
+            if (j == sg.t1 - 1) umma_commit(bar(kOF));
           }
-          umma_commit(bar(kSFull0 + st));
-          if (j == sg.t1 - 1) umma_commit(bar(kQEmpty));
-          if (j > sg.t0 && !(ok = issue_pv(g - 1u, j - 1 == sg.t0))) break;
         }
-        if (!ok) break;
-        if (!(ok = issue_pv(g - 1u, sg.t1 - 1 == sg.t0))) break;
-        umma_commit(bar(kOFull));
         ++nseg;
       }
-      // every MMA issued so far is complete before TMEM is released
-      umma_commit(bar(kMmaDone));
+      umma_commit(bar(kMmaDone));  // every MMA issued so far has finished before TMEM goes
       drain_bar(bar(kMmaDone), 0);
     }
     __syncwarp();
-  } else {
-    // ===================================================== loads
-    const int ptid = threadIdx.x - 160;  // 0..127
-    if (!kSparse) {
-      if (ptid == 0) {
-        SegIter it(p, unit);
-        Seg sg;
-        uint32_t g = 0, nseg = 0;
-        bool ok = true;
-        uint32_t last_q = 0xffffffffu;
-        while (ok && it.next(sg)) {
-          if (!(ok = wait_bar<false>(bar(kQEmpty), (nseg & 1u) ^ 1u, ctl))) break;
-          mbar_arrive_expect_tx(bar(kQFull), nq * kQChunkBytes);
-          const int qy = (sg.b * p.s_q + tok) * kHeads;
-          for (int c = 0; c < nq; ++c)
-            tma_load_2d(sQ + c * kQChunkBytes, &tm_q, (chunk0 + c) * kChunk, qy, bar(kQFull));
-          last_q = nseg;
-          const int* bt_row = p.block_table + static_cast<long long>(sg.b) * p.bt_stride;
-          for (int j = sg.t0; j < sg.t1; ++j, ++g) {
-            const uint32_t st = g & 1u, ph = (g >> 1) & 1u;
-            if (!(ok = wait_bar<false>(bar(kKvEmpty0 + st), ph ^ 1u, ctl))) break;
-            int page = j < p.bt_stride ? bt_row[j] : -1;
-            // an entry outside the pool reads the TMA fill value (zeros)
-            const int y = (page >= 0 && page < p.num_pages) ? page * kPage
-                                                             : static_cast<int>(p.num_pages) * kPage;
-            mbar_arrive_expect_tx(bar(kKvFull0 + st), nq * kKvChunkBytes);
-            for (int c = 0; c < nq; ++c)
-              tma_load_2d(sKv + st * kStageBytes + c * kKvChunkBytes, &tm_kv, (chunk0 + c) * kChunk, y,
-                          bar(kKvFull0 + st));
-          }
-          ++nseg;
+  } else if (warp == 5) {
+    // ================================================= TMA producer (dense)
+    if (!kSparse && lane == 0) {
+      SegIter it(p, unit);
+      Seg sg;
+      Ring3 rs;
+      uint32_t issued = 0;
+      bool ok = true;
+      while (ok && it.next(sg)) {
+        const int* bt_row = p.block_table + static_cast<long long>(sg.b) * p.bt_stride;
+        for (int j = sg.t0; j < sg.t1; ++j, rs.advance()) {
+          if (!(ok = wait_bar<false>(bar(kKE + rs.idx), rs.phase ^ 1u, ctl))) break;
+          const int page = j < p.bt_stride ? bt_row[j] : -1;
+          // an entry outside the pool reads the TMA fill value (zeros)
+          const int y = (page >= 0 && page < p.num_pages) ? page * kPage : static_cast<int>(p.num_pages) * kPage;
+          mbar_arrive_expect_tx(bar(kKF + rs.idx), nchunks * kChunkBytes);
+          for (int c = 0; c < nchunks; ++c)
+            tma_load_2d(sStage + rs.idx * stage_bytes + c * kChunkBytes, &tm_kv, c * kChunk, y, bar(kKF + rs.idx));
+          ++issued;
         }
-        if (!ok) {  // let copies in flight land before the CTA goes away
-          if (last_q != 0xffffffffu) drain_bar(bar(kQFull), last_q & 1u);
-          if (g >= 1) drain_bar(bar(kKvFull0 + ((g - 1) & 1u)), ((g - 1) >> 1) & 1u);
-          if (g >= 2) drain_bar(bar(kKvFull0 + ((g - 2) & 1u)), ((g - 2) >> 1) & 1u);
+      }
+      if (!ok) {  // let copies in flight land before the CTA goes away
+        for (uint32_t k = 0; k < static_cast<uint32_t>(kStages) && k < issued; ++k) {
+          const uint32_t t = issued - 1 - k;
+          drain_bar(bar(kKF + t % kStages), (t / kStages) & 1u);
+        }
+      }
+    }
+  } else {
+    // ================================================= warps 6-9: gather (sparse) / V conversion (O side)
+    const int ptid = threadIdx.x - 192;  // 0..127
+    const int pw = ptid >> 5;
+    SegIter it(p, unit);
+    Seg sg;
+    Ring3 rs;
+    bool ok = true;
+    if (!kSparse && s_side) {
+      // nothing to do: the S side consumes TMA tiles as they land
+    } else if (!kSparse) {
+      // ---- O side, dense: convert the landed bf16 value tile to fp16 * 2^-8 in place
+      while (ok && it.next(sg)) {
+        const int L = max(p.cache_lens[sg.b], 0);
+        for (int j = sg.t0; j < sg.t1; ++j, rs.advance()) {
+          if (!(ok = warp_wait(bar(kKF + rs.idx), rs.phase, ctl))) break;
+          const uint32_t stg = sStage + rs.idx * kStageO;
+          const int r_end = L - j * 64;  // rows >= r_end lie past the cache end: zero them
+#pragma unroll 4
+          for (int i = 0; i < kStageO / 16 / 128; ++i) {
+            const int piece = ptid + 128 * i;
+            const uint32_t a = stg + 16u * piece;
+            const int r = (piece & 511) >> 3;  // the swizzle only permutes pieces within a row
+            if (r >= r_end) {
+              st_shared_zero16(a);
+            } else {
+              uint4 v;
+              asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                           : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a) : "memory");
+              st_shared_v4(a, bf16x2_to_f16x2_scaled(v.x), bf16x2_to_f16x2_scaled(v.y),
+                           bf16x2_to_f16x2_scaled(v.z), bf16x2_to_f16x2_scaled(v.w));
+            }
+          }
+          fence_proxy_async_smem();
+          mbar_arrive(bar(kVR + rs.idx));
         }
       }
     } else {
-      // sparse gather: warp pw fills rows pw*16 .. pw*16+15 of each tile
-      const int pw = ptid >> 5;
-      SegIter it(p, unit);
-      Seg sg;
-      uint32_t g = 0, nseg = 0;
-      bool ok = true;
-      uint32_t last_q = 0xffffffffu;
+      // ---- sparse: gather rows; the O side converts its 512 value dims on the way
       while (ok && it.next(sg)) {
-        if (pw == 0) {  // warp-uniform outcome: the loader warps use warp-collective ops
-          bool qok = true;
-          if (lane == 0) {
-            qok = wait_bar<false>(bar(kQEmpty), (nseg & 1u) ^ 1u, ctl);
-            if (qok) {
-              mbar_arrive_expect_tx(bar(kQFull), nq * kQChunkBytes);
-              const int qy = (sg.b * p.s_q + tok) * kHeads;
-              for (int c = 0; c < nq; ++c)
-                tma_load_2d(sQ + c * kQChunkBytes, &tm_q, (chunk0 + c) * kChunk, qy, bar(kQFull));
-              last_q = nseg;
-            }
-          }
-          if (!(ok = __all_sync(0xffffffffu, qok))) break;
-        }
         const int L = max(p.cache_lens[sg.b], 0);
-        const int* idx = p.topk_idx + (static_cast<long long>(sg.b) * p.s_q + tok) * p.topk;
-        const int* bt_row = p.block_table + static_cast<long long>(sg.b) * p.bt_stride;
-        for (int j = sg.t0; j < sg.t1; ++j, ++g) {
-          const uint32_t st = g & 1u, ph = (g >> 1) & 1u;
-          if (!(ok = __all_sync(0xffffffffu, wait_bar<false>(bar(kKvEmpty0 + st), ph ^ 1u, ctl))))
-            break;
+        const long long bt_row = static_cast<long long>(sg.b) * p.s_q + tok;
+        const int* idx = p.topk_idx + bt_row * p.topk;
+        const int* tbl = p.block_table + static_cast<long long>(sg.b) * p.bt_stride;
+        for (int j = sg.t0; j < sg.t1; ++j, rs.advance()) {
+          if (!(ok = warp_wait(bar(kKE + rs.idx), rs.phase ^ 1u, ctl))) break;
           long long prow = -1;
           {
             const int pos = j * 64 + pw * 16 + (lane & 15);
             if (lane < 16 && pos < p.topk) {
               const int ix = idx[pos];
               if (ix >= 0 && ix < L && (ix >> 6) < p.bt_stride) {
-                const int pg = bt_row[ix >> 6];
+                const int pg = tbl[ix >> 6];
                 if (pg >= 0 && pg < p.num_pages) prow = static_cast<long long>(pg) * kPage + (ix & 63);
               }
             }
           }
-          const uint32_t vbits = __ballot_sync(0xffffffffu, prow >= 0) & 0xffffu;
-          if (lane == 0)
-            *reinterpret_cast<volatile uint16_t*>(smem + kOffMask + 8 * st + 2 * pw) =
-                static_cast<uint16_t>(vbits);
-          const uint32_t stg = sKv + st * kStageBytes;
-          // each lane moves 16-byte pieces; nq * 8 pieces per row
+          const uint32_t stg = sStage + rs.idx * stage_bytes;
           for (int rr = 0; rr < 16; ++rr) {
             const int r = pw * 16 + rr;
             const long long pr = __shfl_sync(0xffffffffu, prow, rr);
-            for (int c16 = lane; c16 < nq * 8; c16 += 32) {
-              const uint32_t dst = stg + (c16 >> 3) * kKvChunkBytes + r * 128 +
-                                   (((c16 & 7) ^ (r & 7)) << 4);
+            for (int c16 = lane; c16 < nchunks * 8; c16 += 32) {
+              const uint32_t dst = stg + (c16 >> 3) * kChunkBytes + r * 128 + (((c16 & 7) ^ (r & 7)) << 4);
               if (pr >= 0) {
-                const uint4 v = *reinterpret_cast<const uint4*>(
-                    p.kv + pr * kDqk + (chunk0 + (c16 >> 3)) * kChunk + (c16 & 7) * 8);
-                st_shared_v4(dst, v.x, v.y, v.z, v.w);
+                const uint4 v = __ldg(reinterpret_cast<const uint4*>(p.kv + pr * kDqk + c16 * 8));
+                if (s_side)
+                  st_shared_v4(dst, v.x, v.y, v.z, v.w);
+                else
+                  st_shared_v4(dst, bf16x2_to_f16x2_scaled(v.x), bf16x2_to_f16x2_scaled(v.y),
+                               bf16x2_to_f16x2_scaled(v.z), bf16x2_to_f16x2_scaled(v.w));
               } else {
                 st_shared_zero16(dst);
               }
             }
           }
           fence_proxy_async_smem();
-          mbar_arrive(bar(kKvFull0 + st));
+          mbar_arrive(bar((s_side ? kKF : kVR) + rs.idx));
         }
-        ++nseg;
       }
-      if (!ok && ptid == 0 && last_q != 0xffffffffu) drain_bar(bar(kQFull), last_q & 1u);
     }
   }
 
@@ -630,12 +748,12 @@ cudaError_t decode_max_clusters(int* n, int num_clusters_hint) {
 }
 
 cudaError_t decode_launch(bool sparse, int num_clusters, cudaStream_t stream, const DecodeParams& p,
-                          const CUtensorMap& tm_q, const CUtensorMap& tm_kv) {
+                          const CUtensorMap& tm_kv) {
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[1];
   cluster_config(cfg, attr, num_clusters, stream);
-  return sparse ? cudaLaunchKernelEx(&cfg, mla_decode_kernel<true>, p, tm_q, tm_kv)
-                : cudaLaunchKernelEx(&cfg, mla_decode_kernel<false>, p, tm_q, tm_kv);
+  return sparse ? cudaLaunchKernelEx(&cfg, mla_decode_kernel<true>, p, tm_kv)
+                : cudaLaunchKernelEx(&cfg, mla_decode_kernel<false>, p, tm_kv);
 }
 
 }  // namespace mla
