@@ -22,11 +22,11 @@ __global__ void mla_validate_kernel(const int* lens, const int* bt, long long bt
                                     long long num_pages, int B, int s_q, const int* topk_idx, int topk,
                                     int* status);
 int decode_smem_bytes();
-int decode_threads();
+int decode_threads(bool sparse);
 cudaError_t decode_set_attrs();
 cudaError_t decode_max_clusters(int* n, int num_clusters_hint);
 cudaError_t decode_launch(bool sparse, int num_clusters, cudaStream_t stream, const DecodeParams& p,
-                          const CUtensorMap& tm_kv);
+                          const CUtensorMap& tm_q, const CUtensorMap& tm_kv);
 }  // namespace mla
 
 using namespace mla;
@@ -211,7 +211,7 @@ int mla_decode(const void* q, const void* kv_cache, int64_t num_pages, const int
   if (flags & ~static_cast<unsigned>(MLA_FLAG_CAUSAL | MLA_FLAG_OUT_FP32 | MLA_FLAG_VALIDATE))
     return MLA_ERR_INVALID_ARG;
   if (num_heads != kHeads || s_q < 1 || s_q > 2) return MLA_ERR_UNSUPPORTED;
-  if (!std::isfinite(softmax_scale)) return MLA_ERR_INVALID_ARG;
+  if (!std::isfinite(softmax_scale) || !(softmax_scale > 0.f)) return MLA_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(out, 16) || !aligned(lse, 4) ||
       !aligned(block_table, 4) || !aligned(cache_lens, 4) || !aligned(workspace, 256) ||
       (topk_idx && !aligned(topk_idx, 4)))
@@ -264,10 +264,11 @@ int mla_decode(const void* q, const void* kv_cache, int64_t num_pages, const int
   p.part_lse = reinterpret_cast<float*>(ws + L.part_lse);
   p.part_o = reinterpret_cast<float*>(ws + L.part_o);
 
-  CUtensorMap tm_kv;
+  CUtensorMap tm_q, tm_kv;
+  if ((rc = encode_2d(&tm_q, q, static_cast<uint64_t>(batch) * s_q * kHeads, kHeads)) != MLA_OK) return rc;
   if ((rc = encode_2d(&tm_kv, kv_cache, static_cast<uint64_t>(num_pages) * kPage, kPage)) != MLA_OK) return rc;
 
-  const cudaError_t e = decode_launch(topk_idx != nullptr, U * s_q, s, p, tm_kv);
+  const cudaError_t e = decode_launch(topk_idx != nullptr, U * s_q, s, p, tm_q, tm_kv);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return MLA_ERR_CUDA;

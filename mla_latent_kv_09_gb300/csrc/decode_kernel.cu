@@ -18,8 +18,8 @@
 //     rescale factor into CTA 1's shared memory with st.async, which
 //     completes on CTA 1's mbarrier (no round trip, no fence).
 //   CTA 1, "O side": owns O (128 x 512 fp32, all 512 TMEM columns); per tile
-//     it converts the value part of the tile to fp16 in shared memory (scaled
-//     by 2^-8 so the fp16 range covers |v| < 2^24), rescales O rows when the
+//     it converts the value part of the tile to fp16 in shared memory (values
+//     must stay below 65504 in magnitude), rescales O rows when the
 //     S side moved the max, and accumulates O += P V on tcgen05 (M=128,
 //     N=2x256, K=64).  P and V in fp16 keep 11 significant bits on the
 //     softmax weights (bf16 would keep 8), which is what holds the O error
@@ -31,9 +31,11 @@
 // partial plus its LSE, merged by the combine kernel (the split-K remedy of
 // "The 31-Millisecond Smoking Gun").
 //
-// Warps (320 threads): 0-3 softmax (S side) / O correction + epilogue (O
-// side), thread i = head row i = TMEM lane i; 4 MMA issue + TMEM owner;
-// 5 TMA producer; 6-9 sparse row gather (S side) / V conversion (O side).
+// Warps (384 threads).  S side: 0-7 softmax (warp w: head rows 32*(w%4)..,
+// columns 32*(w/4).. of each tile), 8 MMA issue + TMEM owner, 9 TMA
+// producer, 10-11 row gather (sparse).  O side: 0-3 O correction + epilogue
+// (thread i = head row i = TMEM lane i), 4-7 V conversion (with 10-11 when
+// dense) or row gather + conversion (sparse), 8 MMA issue, 9 TMA producer.
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -47,6 +49,8 @@ constexpr int kStages = 3;
 constexpr int kStageS = kNumChunks * kChunkBytes;  // 9 chunks: all 576 dims
 constexpr int kStageO = 8 * kChunkBytes;           // 8 chunks: the 512 value dims
 constexpr int kPBytes = kHeads * 128;              // 128 rows x 64 fp16
+constexpr int kQChunkBytes = kHeads * 128;         // Q: 128 rows x 64 bf16, 128B-swizzled
+constexpr int kPrefetch = 4;                       // tiles prefetched into L2 ahead of the TMA
 
 // Shared-memory layout (offsets from a 1024-aligned base).  The barrier block
 // sits at the same offset in both CTAs (multicast commits rely on it).
@@ -55,11 +59,12 @@ constexpr int kOffP = kStages * kStageO;             // O side: 196608
 constexpr int kOffAlpha = kOffP + 2 * kPBytes;       // O side: float[2][128]
 constexpr int kOffFin = kOffAlpha + 2 * kHeads * 4;  // O side: float[2][128]
 constexpr int kOffBar = kOffFin + 2 * kHeads * 4;    // 231424
+constexpr int kOffXchg = kStages * kStageS;          // S side: row max / sum exchange, 4 KiB
 constexpr int kBarBytes = 256;
 constexpr int kSmemUsed = kOffBar + kBarBytes;
 constexpr int kAlignSlack = 768;
 constexpr int kSmemBytes = kSmemUsed + kAlignSlack;  // 232448 = the opt-in maximum
-static_assert(kStages * kStageS <= kOffBar, "S-side stages overlap the barrier block");
+static_assert(kOffXchg + 4096 <= kOffBar, "S-side stages overlap the barrier block");
 
 // Tensor-memory columns.
 constexpr uint32_t kTmemCols = 512;
@@ -67,9 +72,9 @@ constexpr uint32_t kColS = 0;     // S side: two 64-column score buffers
 constexpr uint32_t kColQ = 128;   // S side: Q, 288 columns (576 bf16 packed in pairs)
 constexpr uint32_t kColO = 0;     // O side: O, 512 columns
 
-constexpr int kNumThreads = 320;
+constexpr int kThreads = 384;       // 12 warps
+constexpr int kConvThreads = 192;   // O side, dense: warps 4-7 and 10-11 convert V
 constexpr float kRescaleLog2 = 8.0f;
-constexpr float kVScale = 0.00390625f;  // 2^-8 applied to V in fp16; undone at the end
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 constexpr uint64_t kDrainNs = 20000000ull;
 
@@ -77,18 +82,18 @@ enum Bar {
   kKF = 0,        // [3] tile landed (TMA tx, or 128 gather arrivals)
   kKE = 3,        // [3] tile free (MMA commit)
   kVR = 6,        // [3] O side: fp16 V ready (128 arrivals)
-  kQR = 9,        // S side: Q in TMEM (128 arrivals)
+  kQR = 9,        // (unused)
   kQF = 10,       // S side: Q free (commit after a segment's last QK)
   kSF = 11,       // [2] S side: scores ready (commit)
   kSE = 13,       // [2] S side: scores read (128 arrivals)
   kPFree = 15,    // [2] S side: O side finished PV on that P slot (remote commit)
   kPM = 17,       // [2] O side: P message landed (1 arrival + tx bytes)
   kPR = 19,       // [2] O side: O corrected, PV may go (128 arrivals)
-  kPD = 21,       // O side: a PV finished (commit)
-  kOF = 22,       // O side: segment's last PV finished (commit)
-  kOE = 23,       // O side: epilogue read O (128 arrivals)
-  kMmaDone = 24,  // teardown
-  kNumBars = 25
+  kPD = 21,       // [2] O side: PV of a tile of that parity finished (commit)
+  kOF = 23,       // O side: segment's last PV finished (commit)
+  kOE = 24,       // O side: epilogue read O (128 arrivals)
+  kMmaDone = 25,  // teardown
+  kNumBars = 26
 };
 static_assert(kNumBars * 8 + 16 <= kBarBytes, "barrier block");
 
@@ -175,6 +180,10 @@ __device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity) {
   }
 }
 
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const Ctl& c) {
   return __all_sync(0xffffffffu, wait_bar<false>(bar, parity, c));
 }
@@ -212,20 +221,11 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
-__device__ __forceinline__ float f16_lo(uint32_t v) {
-  float f;
-  asm("{\n .reg .f16 h, x;\n mov.b32 {h, x}, %1;\n cvt.f32.f16 %0, h;\n}" : "=f"(f) : "r"(v));
-  return f;
-}
-__device__ __forceinline__ float f16_hi(uint32_t v) {
-  float f;
-  asm("{\n .reg .f16 h, x;\n mov.b32 {x, h}, %1;\n cvt.f32.f16 %0, h;\n}" : "=f"(f) : "r"(v));
-  return f;
-}
 
-// bf16x2 word -> fp16x2 word of the values times 2^-8.
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2_scaled(uint32_t w) {
-  return pack_f16x2(__uint_as_float(w << 16) * kVScale, __uint_as_float(w & 0xffff0000u) * kVScale);
+// bf16x2 word -> fp16x2 word (exact for |v| in [2^-14, 65504]; smaller values
+// become fp16 subnormals, absolute error <= 2^-25; larger ones overflow).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
+  return pack_f16x2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
 }
 
 // Bytes of one P message (fp16 P tile, per-row rescale, and at the end of a
@@ -235,8 +235,9 @@ __host__ __device__ constexpr uint32_t p_message_bytes(bool last) {
 }
 
 template <bool kSparse>
-__global__ void __launch_bounds__(kNumThreads, 1)
-mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tm_kv) {
+__global__ void __launch_bounds__(kThreads, 1)
+mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tm_q,
+                  const __grid_constant__ CUtensorMap tm_kv) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t mis = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* smem = smem_raw + mis;
@@ -272,31 +273,34 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(bar(kKF + i), kSparse ? 128 : 1);
+      mbar_init(bar(kKF + i), 1);
       mbar_init(bar(kKE + i), 1);
-      mbar_init(bar(kVR + i), 128);
+      mbar_init(bar(kVR + i), kSparse ? 128 : kConvThreads);
     }
-    mbar_init(bar(kQR), 128);
     mbar_init(bar(kQF), 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(kSF + i), 1);
-      mbar_init(bar(kSE + i), 128);
+      mbar_init(bar(kSE + i), 256);
       mbar_init(bar(kPFree + i), 1);
       mbar_init(bar(kPM + i), 1);
       mbar_init(bar(kPR + i), 128);
     }
     mbar_init(bar(kPD), 1);
+    mbar_init(bar(kPD + 1), 1);
     mbar_init(bar(kOF), 1);
     mbar_init(bar(kOE), 128);
     mbar_init(bar(kMmaDone), 1);
     misc[1] = 0u;
     fence_mbar_init();
   }
-  if (warp == 4) {
+  if (warp == 8) {
     tmem_alloc(smem_u32(&misc[0]), kTmemCols);
     tmem_relinquish();
   }
-  if (warp == 5 && lane == 0 && !kSparse) tma_prefetch_desc(&tm_kv);
+  if (warp == 9 && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_kv);
+  }
   tc_fence_before();
   __syncthreads();
   cluster_sync();  // the peer's barriers exist before any remote operation
@@ -309,14 +313,21 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
   ctl.status = p.ws_hdr + kHdrStatus;
   const float NEG_INF = -__int_as_float(0x7f800000);
 
-  if (warp < 4 && s_side) {
+  if (warp < 8 && s_side) {
     // ================================================= S side: Q load + softmax
-    const int row = threadIdx.x;
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    // Warp w handles head rows 32*(w%4) .. +31 (its TMEM lane quarter) and
+    // columns 32*(w/4) .. +31 of every 64-token tile; the two warps of a
+    // quarter swap their partial row max through shared memory.
+    const int q4 = warp & 3, half = warp >> 2;
+    const int row = q4 * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
     const uint32_t rP = mapa(sP, peer) + static_cast<uint32_t>(row) * 128u;
     const uint32_t rAlpha = mapa(sAlpha, peer) + static_cast<uint32_t>(row) * 4u;
     const uint32_t rFin = mapa(sFin, peer) + static_cast<uint32_t>(row) * 4u;
     const uint32_t rPM = mapa(bar(kPM), peer);
+    float* xmax = reinterpret_cast<float*>(smem + kOffXchg);               // [2 parity][2 half][128]
+    float* xsum = reinterpret_cast<float*>(smem + kOffXchg + 4 * kHeads * 4);  // [2 half][2][128]
+    const int pair_bar = 1 + q4;  // named barrier of the two warps of this quarter
     SegIter it(p, unit);
     Seg sg;
     uint32_t g = 0, nseg = 0;
@@ -325,28 +336,9 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
       const int L = max(p.cache_lens[sg.b], 0);
       const int vis = p.causal ? L - p.s_q + tok + 1 : L;
       const long long bt_row = static_cast<long long>(sg.b) * p.s_q + tok;
-      // ---- Q row -> TMEM (after the previous segment's score MMAs)
-      if (!(ok = warp_wait(bar(kQF), (nseg & 1u) ^ 1u, ctl))) break;
-      tc_fence_after();
-      {
-        const uint4* qrow = reinterpret_cast<const uint4*>(p.q + (bt_row * kHeads + row) * kDqk);
-#pragma unroll 1
-        for (int cc = 0; cc < kNumChunks; ++cc) {
-          uint32_t r[32];
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const uint4 v = __ldg(qrow + cc * 8 + k);
-            r[4 * k] = v.x; r[4 * k + 1] = v.y; r[4 * k + 2] = v.z; r[4 * k + 3] = v.w;
-          }
-          tmem_st32(tmem + lane_base + kColQ + 32u * cc, r);
-        }
-        tmem_wait_st();
-      }
-      tc_fence_before();
-      mbar_arrive(bar(kQR));
-
       // z: sum of the fp16-rounded weights (normalises O, whose PV product uses
-      // exactly those weights); zx: sum of the unrounded weights (for the LSE)
+      // exactly those weights); zx: sum of the unrounded weights (for the LSE).
+      // Each half keeps the sums of its own columns.
       float m_used = NEG_INF, z = 0.f, zx = 0.f;
       const int* idx = kSparse ? p.topk_idx + bt_row * p.topk : nullptr;
       for (int j = sg.t0; j < sg.t1; ++j, ++g) {
@@ -354,31 +346,26 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
         const bool last = (j == sg.t1 - 1);
         if (!(ok = warp_wait(bar(kSF + sb), ph, ctl))) break;
         tc_fence_after();
-        float s[64];
+        float s[32];
         {
           uint32_t r[32];
-          tmem_ld32(tmem + lane_base + kColS + 64u * sb, r);
-          uint32_t r2[32];
-          tmem_ld32(tmem + lane_base + kColS + 64u * sb + 32u, r2);
+          tmem_ld32(tmem + lane_base + kColS + 64u * sb + 32u * half, r);
           tmem_wait_ld();
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            s[c] = __uint_as_float(r[c]);
-            s[32 + c] = __uint_as_float(r2[c]);
-          }
+          for (int c = 0; c < 32; ++c) s[c] = __uint_as_float(r[c]);
         }
         tc_fence_before();
         mbar_arrive(bar(kSE + sb));
 
-        // ---- mask, scale to the exp2 domain, tile max
-        float mt = NEG_INF;
+        // ---- mask (masked scores become -inf), then the row max of the raw
+        // scores over both halves (the scale is positive, so max commutes with it)
+        const int col0 = j * 64 + 32 * half;
         if (kSparse) {
-          const int base = j * 64;
           const bool vec = ((p.topk & 3) == 0) && ((reinterpret_cast<uintptr_t>(idx) & 15) == 0);
 #pragma unroll
-          for (int c4 = 0; c4 < 16; ++c4) {
+          for (int c4 = 0; c4 < 8; ++c4) {
             int iv[4];
-            const int pos = base + 4 * c4;
+            const int pos = col0 + 4 * c4;
             if (vec && pos + 3 < p.topk) {
               const int4 v = __ldg(reinterpret_cast<const int4*>(idx + pos));
               iv[0] = v.x; iv[1] = v.y; iv[2] = v.z; iv[3] = v.w;
@@ -389,20 +376,27 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
               const bool valid = iv[k] >= 0 && iv[k] < L;
-              const float t = valid ? s[4 * c4 + k] * p.scale_log2 : NEG_INF;
-              s[4 * c4 + k] = t;
-              mt = fmaxf(mt, t);
+              s[4 * c4 + k] = valid ? s[4 * c4 + k] : NEG_INF;
             }
           }
         } else {
-          const int nvalid = vis - j * 64;
+          const int nvalid = vis - col0;
+          if (nvalid < 32) {
 #pragma unroll
-          for (int c = 0; c < 64; ++c) {
-            const float t = c < nvalid ? s[c] * p.scale_log2 : NEG_INF;
-            s[c] = t;
-            mt = fmaxf(mt, t);
+            for (int c = 0; c < 32; ++c) s[c] = c < nvalid ? s[c] : NEG_INF;
           }
         }
+        float mh;
+        {
+          float m4[4] = {NEG_INF, NEG_INF, NEG_INF, NEG_INF};
+#pragma unroll
+          for (int c = 0; c < 32; ++c) m4[c & 3] = fmaxf(m4[c & 3], s[c]);
+          mh = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+        }
+        float* xm = xmax + (sb * 2) * kHeads;
+        xm[half * kHeads + row] = mh;
+        named_bar_sync(pair_bar, 64);
+        const float mt = fmaxf(mh, xm[(half ^ 1) * kHeads + row]) * p.scale_log2;  // same in both halves
 
         // ---- online softmax with a lazy rescale of the reference max
         float alpha = 1.f;
@@ -412,22 +406,28 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
           z *= alpha;
           zx *= alpha;
         }
-        uint32_t pk[32];
+        uint32_t pk[16];
         if (m_used == NEG_INF) {
 #pragma unroll
-          for (int c = 0; c < 32; ++c) pk[c] = 0u;
+          for (int c = 0; c < 16; ++c) pk[c] = 0u;
         } else {
-          float zs = 0.f, ze = 0.f;
+          // P = 2^(s * scale_log2 - m) in one FFMA + EX2; the fp16-rounded
+          // weights are summed exactly by reading each fp16 pattern as an fp32
+          // pattern shifted by 13 bits, which is the same value times 2^-112
+          // (normal and subnormal alike); the 2^112 is applied once per tile
+          float zs[4] = {0.f, 0.f, 0.f, 0.f}, ze[4] = {0.f, 0.f, 0.f, 0.f};
+          const float nm = -m_used;
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const float p0 = ex2_approx(s[2 * c] - m_used);
-            const float p1 = ex2_approx(s[2 * c + 1] - m_used);
+          for (int c = 0; c < 16; ++c) {
+            const float p0 = ex2_approx(fmaf(s[2 * c], p.scale_log2, nm));
+            const float p1 = ex2_approx(fmaf(s[2 * c + 1], p.scale_log2, nm));
             pk[c] = pack_f16x2(p0, p1);
-            zs += f16_lo(pk[c]) + f16_hi(pk[c]);
-            ze += p0 + p1;
+            zs[c & 3] += __uint_as_float((pk[c] << 13) & 0x0fffe000u) +
+                         __uint_as_float((pk[c] >> 3) & 0x0fffe000u);
+            ze[c & 3] += p0 + p1;
           }
-          z += zs;
-          zx += ze;
+          z += ((zs[0] + zs[1]) + (zs[2] + zs[3])) * 5.192296858534828e33f;  // 2^112
+          zx += (ze[0] + ze[1]) + (ze[2] + ze[3]);
         }
 
         // ---- P message to the O side, once it is done with this slot
@@ -435,20 +435,29 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
         const uint32_t mbar = rPM + 8u * sb;
         const uint32_t prow = rP + sb * kPBytes;
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-          st_async_v4(prow + ((static_cast<uint32_t>(k) ^ (row & 7)) << 4), pk[4 * k], pk[4 * k + 1],
-                      pk[4 * k + 2], pk[4 * k + 3], mbar);
-        st_async_b32(rAlpha + sb * kHeads * 4u, __float_as_uint(alpha), mbar);
-        if (last) {
-          // O_final = O_acc * 2^8 / z (the 2^8 undoes the scaling of V)
-          const float fin = z > 0.f ? 256.f / z : 0.f;
-          st_async_b32(rFin + sb * kHeads * 4u, __float_as_uint(fin), mbar);
-          const float lse = zx > 0.f ? (m_used + log2f(zx)) * 0.69314718055994531f : NEG_INF;
-          if (sg.slot < 0) {
-            p.lse[bt_row * kHeads + row] = lse;
-          } else if (sg.slot < 2 * U) {  // the plan never uses more than 2 * (U - 1) slots
-            p.part_lse[(static_cast<long long>(sg.slot) * p.s_q + tok) * kHeads + row] = lse;
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t piece = static_cast<uint32_t>(4 * half + k);
+          st_async_v4(prow + ((piece ^ (row & 7)) << 4), pk[4 * k], pk[4 * k + 1], pk[4 * k + 2],
+                      pk[4 * k + 3], mbar);
+        }
+        if (half == 0) st_async_b32(rAlpha + sb * kHeads * 4u, __float_as_uint(alpha), mbar);
+        if (last) {  // ---- segment end: both halves' sums -> final scale and LSE
+          xsum[(half * 2 + 0) * kHeads + row] = z;
+          xsum[(half * 2 + 1) * kHeads + row] = zx;
+          named_bar_sync(pair_bar, 64);
+          if (half == 0) {
+            const float zt = z + xsum[(2 + 0) * kHeads + row];
+            const float zxt = zx + xsum[(2 + 1) * kHeads + row];
+            const float fin = zt > 0.f ? 1.f / zt : 0.f;  // O_final = O_acc / z
+            st_async_b32(rFin + sb * kHeads * 4u, __float_as_uint(fin), mbar);
+            const float lse = zxt > 0.f ? (m_used + log2f(zxt)) * 0.69314718055994531f : NEG_INF;
+            if (sg.slot < 0) {
+              p.lse[bt_row * kHeads + row] = lse;
+            } else if (sg.slot < 2 * U) {  // the plan never uses more than 2 * (U - 1) slots
+              p.part_lse[(static_cast<long long>(sg.slot) * p.s_q + tok) * kHeads + row] = lse;
+            }
           }
+          named_bar_sync(pair_bar, 64);  // xsum is reused at the next segment end
         }
       }
       ++nseg;
@@ -474,7 +483,10 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
         if (last) fin = fin_s[pb * kHeads + row];
         const bool resc = (j != sg.t0) && alpha != 1.f;
         if (__any_sync(0xffffffffu, resc)) {  // tcgen05.ld/st are warp-collective
-          if (!(ok = warp_wait(bar(kPD), (g - 1u) & 1u, ctl))) break;
+          // PV(g-1) finished: phase (g-1)/2 of the barrier of its parity (the
+          // phase before it, PV(g-3), is known complete: P(g-1) was sent after it)
+          const uint32_t gp = g - 1u;
+          if (!(ok = warp_wait(bar(kPD + (gp & 1u)), (gp >> 1) & 1u, ctl))) break;
           tc_fence_after();
           const float a = resc ? alpha : 1.f;
 #pragma unroll 1
@@ -535,7 +547,7 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
       }
       ++nseg;
     }
-  } else if (warp == 4) {
+  } else if (warp == 8) {
     // ================================================= MMA issue (one thread)
     if (lane == 0) {
       SegIter it(p, unit);
@@ -545,8 +557,24 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
       bool ok = true;
       while (ok && it.next(sg)) {
         if (s_side) {
-          if (!(ok = wait_bar<false>(bar(kQR), nseg & 1u, ctl))) break;
-          tc_fence_after();
+          // Q of this segment arrives as three ring slots of three 64-dim chunks
+          // (16 KiB each, 128-byte swizzled); tcgen05.cp moves them into TMEM
+          // once the previous segment's score MMAs have read the old Q
+          if (nseg > 0 && !(ok = wait_bar<false>(bar(kQF), (nseg - 1u) & 1u, ctl))) break;
+          for (int k = 0; k < 3 && ok; ++k, rs.advance()) {
+            if (!(ok = wait_bar<false>(bar(kKF + rs.idx), rs.phase, ctl))) break;
+            tc_fence_after();
+            const uint64_t qd0 = smem_desc(sStage + rs.idx * stage_bytes, 16u, 1024u);
+#pragma unroll
+            for (int i = 0; i < 3; ++i) {
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                tmem_cp_128x256b(tmem + kColQ + 32u * (3 * k + i) + 8u * kk,
+                                 qd0 + static_cast<uint64_t>((i * kQChunkBytes + 32 * kk) >> 4));
+            }
+            umma_commit(bar(kKE + rs.idx));
+          }
+          if (!ok) break;
         }
         for (int j = sg.t0; j < sg.t1; ++j, ++g, rs.advance()) {
           const uint32_t stg = sStage + rs.idx * stage_bytes;
@@ -555,13 +583,17 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
             if (!(ok = wait_bar<false>(bar(kKF + rs.idx), rs.phase, ctl))) break;
             if (!(ok = wait_bar<false>(bar(kSE + sb), ph ^ 1u, ctl))) break;
             tc_fence_after();
+            // 36 MMAs (K = 576 in steps of 16): descriptors differ from the
+            // tile's base descriptor by compile-time offsets
+            const uint64_t bd0 = smem_desc(stg, 16u, 1024u);
+            const uint32_t dS = tmem + kColS + 64u * sb;
+#pragma unroll
             for (int c = 0; c < kNumChunks; ++c) {
 #pragma unroll
-              for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t bd = smem_desc(stg + c * kChunkBytes + 32u * kk, 16u, 1024u);
-                umma_f16_tmem_a(tmem + kColS + 64u * sb, tmem + kColQ + 32u * c + 8u * kk, bd, kIdescQK,
+              for (int kk = 0; kk < 4; ++kk)
+                umma_f16_tmem_a(dS, tmem + kColQ + 32u * c + 8u * kk,
+                                bd0 + static_cast<uint64_t>((c * kChunkBytes + 32 * kk) >> 4), kIdescQK,
                                 (c | kk) != 0 ? 1u : 0u);
-              }
             }
             umma_commit(bar(kSF + sb));
             umma_commit(bar(kKE + rs.idx));
@@ -572,18 +604,20 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
             if (!(ok = wait_bar<false>(bar(kPR + sb), ph, ctl))) break;
             if (first && !(ok = wait_bar<false>(bar(kOE), (nseg & 1u) ^ 1u, ctl))) break;
             tc_fence_after();
+            const uint64_t ad0 = smem_desc(sP + sb * kPBytes, 16u, 1024u);
+            const uint64_t bd0 = smem_desc(stg, 8192u, 1024u);  // V, MN-major
+            const uint32_t acc0 = first ? 0u : 1u;
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t ad = smem_desc(sP + sb * kPBytes + 32u * kk, 16u, 1024u);
 #pragma unroll
-              for (int h = 0; h < 2; ++h) {
-                const uint64_t bd = smem_desc(stg + h * 4 * kChunkBytes + 2048u * kk, 8192u, 1024u);
-                umma_f16(tmem + kColO + 256u * h, ad, bd, kIdescPV, (first && kk == 0) ? 0u : 1u);
-              }
+              for (int h = 0; h < 2; ++h)
+                umma_f16(tmem + kColO + 256u * h, ad0 + static_cast<uint64_t>((32 * kk) >> 4),
+                         bd0 + static_cast<uint64_t>((h * 4 * kChunkBytes + 2048 * kk) >> 4), kIdescPV,
+                         kk == 0 ? acc0 : 1u);
             }
             umma_commit(bar(kKE + rs.idx));
             umma_commit_multicast(bar(kPFree + sb), 1);  // the S side may reuse this P slot
-            umma_commit(bar(kPD));
+            umma_commit(bar(kPD + sb));
             if (j == sg.t1 - 1) umma_commit(bar(kOF));
           }
         }
@@ -593,65 +627,111 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
       drain_bar(bar(kMmaDone), 0);
     }
     __syncwarp();
-  } else if (warp == 5) {
-    // ================================================= TMA producer (dense)
-    if (!kSparse && lane == 0) {
-      SegIter it(p, unit);
-      Seg sg;
-      Ring3 rs;
-      uint32_t issued = 0;
-      bool ok = true;
-      while (ok && it.next(sg)) {
-        const int* bt_row = p.block_table + static_cast<long long>(sg.b) * p.bt_stride;
-        for (int j = sg.t0; j < sg.t1; ++j, rs.advance()) {
-          if (!(ok = wait_bar<false>(bar(kKE + rs.idx), rs.phase ^ 1u, ctl))) break;
-          const int page = j < p.bt_stride ? bt_row[j] : -1;
-          // an entry outside the pool reads the TMA fill value (zeros)
-          const int y = (page >= 0 && page < p.num_pages) ? page * kPage : static_cast<int>(p.num_pages) * kPage;
-          mbar_arrive_expect_tx(bar(kKF + rs.idx), nchunks * kChunkBytes);
-          for (int c = 0; c < nchunks; ++c)
-            tma_load_2d(sStage + rs.idx * stage_bytes + c * kChunkBytes, &tm_kv, c * kChunk, y, bar(kKF + rs.idx));
+  } else if (warp == 9) {
+    // ================================================= TMA producer (whole warp; lane 0 issues)
+    // S side: per segment three Q slots, then (dense) one slot per tile.  O
+    // side (dense): one slot per tile, value dims only.  Page ids are read 32
+    // at a time with one coalesced load; the S side also prefetches the pages
+    // of tiles kPrefetch ahead into L2.
+    SegIter it(p, unit);
+    Seg sg;
+    Ring3 rs;
+    uint32_t issued = 0;
+    bool ok = true;
+    // in sparse mode the gather warps are the only filler of the ring (the S
+    // side's gather warps load Q too): a ring shared by two fillers could let
+    // one of them drift a whole lap, which mbarrier parity waits cannot see
+    while (!kSparse && ok && it.next(sg)) {
+      if (s_side) {
+        const int qy = (sg.b * p.s_q + tok) * kHeads;
+        for (int k = 0; k < 3 && ok; ++k, rs.advance()) {
+          if (!(ok = warp_wait(bar(kKE + rs.idx), rs.phase ^ 1u, ctl))) break;
+          if (lane == 0) {
+            mbar_arrive_expect_tx(bar(kKF + rs.idx), 3 * kQChunkBytes);
+            for (int i = 0; i < 3; ++i)
+              tma_load_2d(sStage + rs.idx * stage_bytes + i * kQChunkBytes, &tm_q, (3 * k + i) * kChunk, qy,
+                          bar(kKF + rs.idx));
+          }
+          ++issued;
+        }
+        if (!ok) break;
+      }
+      const int* bt_row = p.block_table + static_cast<long long>(sg.b) * p.bt_stride;
+      for (int jb = sg.t0; jb < sg.t1 && ok; jb += 32) {
+        const int cnt = min(32, sg.t1 - jb);
+        int my_page = -1;
+        if (lane < cnt && jb + lane < p.bt_stride) {
+          const int pg = bt_row[jb + lane];
+          my_page = (pg >= 0 && pg < p.num_pages) ? pg : -1;
+        }
+        if (s_side && lane < kPrefetch && lane < cnt && my_page >= 0)
+          bulk_prefetch_l2(p.kv + static_cast<long long>(my_page) * kPage * kDqk, kPage * kDqk * 2);
+        for (int jj = 0; jj < cnt; ++jj, rs.advance()) {
+          const int page = __shfl_sync(0xffffffffu, my_page, jj);
+          const int pf = __shfl_sync(0xffffffffu, my_page, min(jj + kPrefetch, 31));
+          if (!(ok = warp_wait(bar(kKE + rs.idx), rs.phase ^ 1u, ctl))) break;
+          if (lane == 0) {
+            if (s_side && jj + kPrefetch < cnt && pf >= 0)
+              bulk_prefetch_l2(p.kv + static_cast<long long>(pf) * kPage * kDqk, kPage * kDqk * 2);
+            // an entry outside the pool reads the TMA fill value (zeros)
+            const int y = page >= 0 ? page * kPage : static_cast<int>(p.num_pages) * kPage;
+            mbar_arrive_expect_tx(bar(kKF + rs.idx), nchunks * kChunkBytes);
+            for (int c = 0; c < nchunks; ++c)
+              tma_load_2d(sStage + rs.idx * stage_bytes + c * kChunkBytes, &tm_kv, c * kChunk, y,
+                          bar(kKF + rs.idx));
+          }
           ++issued;
         }
       }
-      if (!ok) {  // let copies in flight land before the CTA goes away
-        for (uint32_t k = 0; k < static_cast<uint32_t>(kStages) && k < issued; ++k) {
-          const uint32_t t = issued - 1 - k;
-          drain_bar(bar(kKF + t % kStages), (t / kStages) & 1u);
-        }
+    }
+    if (!ok && lane == 0) {  // let copies in flight land before the CTA goes away
+      for (uint32_t k = 0; k < static_cast<uint32_t>(kStages) && k < issued; ++k) {
+        const uint32_t t = issued - 1 - k;
+        drain_bar(bar(kKF + t % kStages), (t / kStages) & 1u);
       }
     }
   } else {
-    // ================================================= warps 6-9: gather (sparse) / V conversion (O side)
-    const int ptid = threadIdx.x - 192;  // 0..127
-    const int pw = ptid >> 5;
+    // ================================================= O side warps 4-7 (+10-11 dense): V conversion
+    // (dense) or gather + conversion (sparse); S side warps 10-11: gather (sparse)
+    const int ptid = s_side ? threadIdx.x - 320 : (warp < 8 ? threadIdx.x - 128 : threadIdx.x - 192);
     SegIter it(p, unit);
     Seg sg;
     Ring3 rs;
     bool ok = true;
-    if (!kSparse && s_side) {
+    if ((!kSparse && s_side) || (kSparse && !s_side && warp >= 10)) {
       // nothing to do: the S side consumes TMA tiles as they land
     } else if (!kSparse) {
-      // ---- O side, dense: convert the landed bf16 value tile to fp16 * 2^-8 in place
+      // ---- O side, dense: 192 threads convert the landed bf16 value tile to fp16 in place
+      constexpr int kPieces = kStageO / 16;  // 4096 pieces of 16 B
       while (ok && it.next(sg)) {
         const int L = max(p.cache_lens[sg.b], 0);
         for (int j = sg.t0; j < sg.t1; ++j, rs.advance()) {
           if (!(ok = warp_wait(bar(kKF + rs.idx), rs.phase, ctl))) break;
           const uint32_t stg = sStage + rs.idx * kStageO;
           const int r_end = L - j * 64;  // rows >= r_end lie past the cache end: zero them
+          if (r_end >= 64) {
 #pragma unroll 4
-          for (int i = 0; i < kStageO / 16 / 128; ++i) {
-            const int piece = ptid + 128 * i;
-            const uint32_t a = stg + 16u * piece;
-            const int r = (piece & 511) >> 3;  // the swizzle only permutes pieces within a row
-            if (r >= r_end) {
-              st_shared_zero16(a);
-            } else {
+            for (int piece = ptid; piece < kPieces; piece += kConvThreads) {
+              const uint32_t a = stg + 16u * piece;
               uint4 v;
               asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
                            : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a) : "memory");
-              st_shared_v4(a, bf16x2_to_f16x2_scaled(v.x), bf16x2_to_f16x2_scaled(v.y),
-                           bf16x2_to_f16x2_scaled(v.z), bf16x2_to_f16x2_scaled(v.w));
+              st_shared_v4(a, bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z),
+                           bf16x2_to_f16x2(v.w));
+            }
+          } else {
+            for (int piece = ptid; piece < kPieces; piece += kConvThreads) {
+              const uint32_t a = stg + 16u * piece;
+              const int r = (piece & 511) >> 3;  // the swizzle only permutes pieces within a row
+              if (r >= r_end) {
+                st_shared_zero16(a);
+              } else {
+                uint4 v;
+                asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                             : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a) : "memory");
+                st_shared_v4(a, bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z),
+                             bf16x2_to_f16x2(v.w));
+              }
             }
           }
           fence_proxy_async_smem();
@@ -659,8 +739,27 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
         }
       }
     } else {
-      // ---- sparse: gather rows; the O side converts its 512 value dims on the way
+      // ---- sparse: each S-side thread gathers one row (all 576 dims), each
+      // pair of O-side threads one row's 512 value dims (which they then
+      // convert to fp16 in place); rows the list does not name are zero-filled
+      const int nthreads = s_side ? 64 : 128;
+      const int r = s_side ? ptid : (ptid >> 1);
+      const int pc0 = s_side ? 0 : (ptid & 1) * 32;          // first 16-byte piece of the row
+      const int npc = s_side ? kNumChunks * 8 : 32;           // pieces this thread moves
       while (ok && it.next(sg)) {
+        if (s_side) {  // three Q slots (TMA, issued by one gather thread)
+          const int qy = (sg.b * p.s_q + tok) * kHeads;
+          for (int k = 0; k < 3 && ok; ++k, rs.advance()) {
+            if (!(ok = warp_wait(bar(kKE + rs.idx), rs.phase ^ 1u, ctl))) break;
+            if (ptid == 0) {
+              mbar_arrive_expect_tx(bar(kKF + rs.idx), 3 * kQChunkBytes);
+              for (int i = 0; i < 3; ++i)
+                tma_load_2d(sStage + rs.idx * stage_bytes + i * kQChunkBytes, &tm_q, (3 * k + i) * kChunk, qy,
+                            bar(kKF + rs.idx));
+            }
+          }
+          if (!ok) break;
+        }
         const int L = max(p.cache_lens[sg.b], 0);
         const long long bt_row = static_cast<long long>(sg.b) * p.s_q + tok;
         const int* idx = p.topk_idx + bt_row * p.topk;
@@ -668,36 +767,44 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
         for (int j = sg.t0; j < sg.t1; ++j, rs.advance()) {
           if (!(ok = warp_wait(bar(kKE + rs.idx), rs.phase ^ 1u, ctl))) break;
           long long prow = -1;
-          {
-            const int pos = j * 64 + pw * 16 + (lane & 15);
-            if (lane < 16 && pos < p.topk) {
-              const int ix = idx[pos];
-              if (ix >= 0 && ix < L && (ix >> 6) < p.bt_stride) {
-                const int pg = tbl[ix >> 6];
-                if (pg >= 0 && pg < p.num_pages) prow = static_cast<long long>(pg) * kPage + (ix & 63);
-              }
+          const int pos = j * 64 + r;
+          if (pos < p.topk) {
+            const int ix = idx[pos];
+            if (ix >= 0 && ix < L && (ix >> 6) < p.bt_stride) {
+              const int pg = tbl[ix >> 6];
+              if (pg >= 0 && pg < p.num_pages) prow = static_cast<long long>(pg) * kPage + (ix & 63);
             }
           }
           const uint32_t stg = sStage + rs.idx * stage_bytes;
-          for (int rr = 0; rr < 16; ++rr) {
-            const int r = pw * 16 + rr;
-            const long long pr = __shfl_sync(0xffffffffu, prow, rr);
-            for (int c16 = lane; c16 < nchunks * 8; c16 += 32) {
-              const uint32_t dst = stg + (c16 >> 3) * kChunkBytes + r * 128 + (((c16 & 7) ^ (r & 7)) << 4);
-              if (pr >= 0) {
-                const uint4 v = __ldg(reinterpret_cast<const uint4*>(p.kv + pr * kDqk + c16 * 8));
-                if (s_side)
-                  st_shared_v4(dst, v.x, v.y, v.z, v.w);
-                else
-                  st_shared_v4(dst, bf16x2_to_f16x2_scaled(v.x), bf16x2_to_f16x2_scaled(v.y),
-                               bf16x2_to_f16x2_scaled(v.z), bf16x2_to_f16x2_scaled(v.w));
-              } else {
-                st_shared_zero16(dst);
-              }
+          const uint16_t* src = p.kv + (prow >= 0 ? prow : 0) * kDqk;
+          const uint32_t src_bytes = prow >= 0 ? 16u : 0u;  // 0: the copy writes zeros
+#pragma unroll 8
+          for (int c = 0; c < npc; ++c) {
+            const int c16 = pc0 + c;
+            cp_async_16_zfill(stg + (c16 >> 3) * kChunkBytes + r * 128 + (((c16 & 7) ^ (r & 7)) << 4),
+                              src + c16 * 8, src_bytes);
+          }
+          cp_async_commit();
+          cp_async_wait<0>();
+          if (!s_side) {  // convert the pieces this thread brought in
+#pragma unroll 8
+            for (int c = 0; c < npc; ++c) {
+              const int c16 = pc0 + c;
+              const uint32_t a = stg + (c16 >> 3) * kChunkBytes + r * 128 + (((c16 & 7) ^ (r & 7)) << 4);
+              uint4 v;
+              asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                           : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a) : "memory");
+              st_shared_v4(a, bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z),
+                           bf16x2_to_f16x2(v.w));
             }
           }
           fence_proxy_async_smem();
-          mbar_arrive(bar((s_side ? kKF : kVR) + rs.idx));
+          if (s_side) {
+            named_bar_sync(5, nthreads);
+            if (ptid == 0) mbar_arrive(bar(kKF + rs.idx));
+          } else {
+            mbar_arrive(bar(kVR + rs.idx));
+          }
         }
       }
     }
@@ -707,7 +814,7 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
   tc_fence_before();
   __syncthreads();
   cluster_sync();  // the peer no longer touches this CTA's shared memory
-  if (warp == 4) {
+  if (warp == 8) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -715,7 +822,7 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
 
 // ------------------------------------------------------------------ host side
 int decode_smem_bytes() { return kSmemBytes; }
-int decode_threads() { return kNumThreads; }
+int decode_threads(bool) { return kThreads; }
 
 cudaError_t decode_set_attrs() {
   cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -725,10 +832,10 @@ cudaError_t decode_set_attrs() {
 }
 
 static void cluster_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, int num_clusters,
-                           cudaStream_t stream) {
+                           cudaStream_t stream, bool sparse) {
   cfg = cudaLaunchConfig_t{};
   cfg.gridDim = dim3(2 * num_clusters, 1, 1);
-  cfg.blockDim = dim3(kNumThreads, 1, 1);
+  cfg.blockDim = dim3(decode_threads(sparse), 1, 1);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -743,17 +850,17 @@ static void cluster_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, i
 cudaError_t decode_max_clusters(int* n, int num_clusters_hint) {
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[1];
-  cluster_config(cfg, attr, num_clusters_hint, nullptr);
+  cluster_config(cfg, attr, num_clusters_hint, nullptr, false);
   return cudaOccupancyMaxActiveClusters(n, mla_decode_kernel<false>, &cfg);
 }
 
 cudaError_t decode_launch(bool sparse, int num_clusters, cudaStream_t stream, const DecodeParams& p,
-                          const CUtensorMap& tm_kv) {
+                          const CUtensorMap& tm_q, const CUtensorMap& tm_kv) {
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[1];
-  cluster_config(cfg, attr, num_clusters, stream);
-  return sparse ? cudaLaunchKernelEx(&cfg, mla_decode_kernel<true>, p, tm_kv)
-                : cudaLaunchKernelEx(&cfg, mla_decode_kernel<false>, p, tm_kv);
+  cluster_config(cfg, attr, num_clusters, stream, sparse);
+  return sparse ? cudaLaunchKernelEx(&cfg, mla_decode_kernel<true>, p, tm_q, tm_kv)
+                : cudaLaunchKernelEx(&cfg, mla_decode_kernel<false>, p, tm_q, tm_kv);
 }
 
 }  // namespace mla
