@@ -178,6 +178,31 @@ int mla_combine(void* workspace, size_t ws_bytes, int batch, int s_q,
  */
 int mla_workspace_status(const void* workspace, mla_stream_t stream);
 
+/*
+ * The same decode step (plan + attention + combine) for callers that cannot
+ * allocate device memory when it runs: a runtime that records its per-token
+ * work into a CUDA graph (allocation is not allowed during stream capture),
+ * or a host program with a fixed device-memory budget that forbids any
+ * allocation after start-up.  There is no counterpart of this call in the
+ * method's description; it only changes where the workspace lives.
+ *
+ * Arguments are those of mla_decode, without workspace and num_units.  The
+ * workspace is a 48 MiB array inside the library's device image, which every
+ * GPU that loads the library keeps until the process exits.  The number of
+ * work units is mla_default_num_units(s_q), lowered if the workspace of
+ * (batch, s_q) would not fit; MLA_ERR_WORKSPACE if it does not fit even with
+ * one unit.  The call allocates nothing.  Its first call on a device looks up
+ * the array's device address (with that device current); make that first
+ * call before any stream capture.  All calls share the array: calls whose
+ * work overlaps on the GPU (other streams, other host threads) race and must
+ * be serialised by the caller.
+ */
+int mla_decode_noalloc(const void* q, const void* kv_cache, int64_t num_pages,
+                       const int32_t* block_table, int64_t bt_stride,
+                       const int32_t* cache_lens, int batch, int s_q, int num_heads,
+                       float softmax_scale, const int32_t* topk_idx, int topk,
+                       unsigned flags, void* out, float* lse, mla_stream_t stream);
+
 /* Human-readable name of a status code (static string). */
 const char* mla_status_string(int status);
 

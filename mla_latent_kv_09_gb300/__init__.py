@@ -33,6 +33,7 @@ from ._binding import (  # noqa: F401
     load,
     mla_combine,
     mla_decode,
+    mla_decode_noalloc,
     mla_decode_plan,
     mla_decode_plan_host,
     mla_decode_workspace_size,

@@ -40,6 +40,8 @@ SIGNATURES = {
                             _uint, _c_int, _vp, _c_size, _vp, _vp, _vp]),
     "mla_combine": (_c_int, [_vp, _c_size, _c_int, _c_int, _c_int, _uint, _c_int, _vp, _vp, _vp]),
     "mla_workspace_status": (_c_int, [_vp, _vp]),
+    "mla_decode_noalloc": (_c_int, [_vp, _vp, _i64, _vp, _i64, _vp, _c_int, _c_int, _c_int, _f32, _vp, _c_int,
+                                    _uint, _vp, _vp, _vp]),
     "mla_status_string": (ctypes.c_char_p, [_c_int]),
 }
 
@@ -146,6 +148,16 @@ def mla_combine(workspace, ws_bytes: int, batch: int, s_q: int, num_heads: int, 
     _check("mla_combine", load().mla_combine(
         _ptr(workspace), int(ws_bytes), int(batch), int(s_q), int(num_heads), int(flags),
         int(num_units), _ptr(out), _ptr(lse), _stream(stream)))
+
+
+def mla_decode_noalloc(q, kv_cache, num_pages: int, block_table, bt_stride: int, cache_lens, batch: int,
+                       s_q: int, num_heads: int, softmax_scale: float, topk_idx, topk: int, flags: int,
+                       out, lse, stream=None) -> None:
+    """The decode step with the library's built-in workspace (allocates nothing)."""
+    _check("mla_decode_noalloc", load().mla_decode_noalloc(
+        _ptr(q), _ptr(kv_cache), int(num_pages), _ptr(block_table), int(bt_stride), _ptr(cache_lens),
+        int(batch), int(s_q), int(num_heads), float(softmax_scale), _ptr(topk_idx), int(topk), int(flags),
+        _ptr(out), _ptr(lse), _stream(stream)))
 
 
 def mla_workspace_status(workspace, stream=None) -> int:
