@@ -74,16 +74,23 @@ typedef enum {
 enum {
   MLA_FLAG_CAUSAL = 1,   /* s_q = 2 MTP decode: token t sees [0, len - s_q + t] */
   MLA_FLAG_OUT_FP32 = 2, /* O is written as fp32 instead of bf16           */
-  MLA_FLAG_VALIDATE = 4  /* check table / lengths / indices first (syncs)   */
+  MLA_FLAG_VALIDATE = 4, /* check table / lengths / indices first (syncs)   */
+  MLA_FLAG_BF16_PV = 8   /* s_q = 2 dense only: the value product takes the
+                            softmax weights and values in bf16 (8 significant
+                            bits on the weights) instead of fp16 (11 bits);
+                            skips converting V; ignored elsewhere          */
 };
 
 enum { MLA_NUM_HEADS = 128, MLA_D_QK = 576, MLA_D_V = 512, MLA_PAGE = 64 };
 
 /*
- * Number of persistent work units (one unit = one pair of SMs working as a
- * 2-CTA cluster) per query token that `num_units = 0` selects on the current
- * device: the number of co-resident 2-CTA clusters divided by s_q.
- * Host-only; returns 0 and sets *err on failure (err may be NULL).
+ * Number of persistent work units that `num_units = 0` selects on the
+ * current device.  s_q = 1: one unit is a pair of SMs working as a 2-CTA
+ * cluster, and the count is the number of co-resident 2-CTA clusters.
+ * s_q = 2: a dense unit is a 4-CTA cluster (two SM pairs) serving both query
+ * tokens, a top-k unit is two 2-CTA clusters (one per token); the count is
+ * what both forms keep resident.  Host-only; returns 0 and sets *err on
+ * failure (err may be NULL).
  */
 int mla_default_num_units(int s_q, int* err);
 
@@ -105,7 +112,8 @@ size_t mla_decode_workspace_size(int batch, int s_q, int num_heads, int num_unit
  *               (every request then has ceil(topk / 64) tiles)
  *   num_units   as for mla_decode_workspace_size
  *   workspace   device buffer of ws_bytes >= mla_decode_workspace_size(...)
- * The work of request b is ceil(len_b / 64) tiles of 64 tokens; the tiles
+ * The work of request b is ceil(len_b / R) tiles of R tokens (R = 128 for
+ * s_q = 2 dense, whose kernel takes two pages per step; else 64); the tiles
  * of all requests, each request charged a fixed per-split overhead, are cut
  * into num_units contiguous, equally loaded ranges.  Requests that straddle
  * a cut are "split" and finish in mla_combine.
@@ -123,8 +131,9 @@ int mla_decode_plan(const int32_t* cache_lens, int batch, int s_q, int topk,
  * unit_meta holds 5 * num_units ints and req_meta 4 * batch ints (host
  * memory, caller-owned).  num_units must be >= 1 here.
  */
-int mla_decode_plan_host(const int32_t* cache_lens_host, int batch, int topk,
-                         int num_units, int32_t* unit_meta, int32_t* req_meta);
+int mla_decode_plan_host(const int32_t* cache_lens_host, int batch, int s_q,
+                         int topk, int num_units, int32_t* unit_meta,
+                         int32_t* req_meta);
 
 /*
  * Attention for one decode step (after mla_decode_plan on the same stream).

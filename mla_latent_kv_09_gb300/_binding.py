@@ -27,6 +27,7 @@ MLA_ERR_TIMEOUT = 8
 MLA_FLAG_CAUSAL = 1
 MLA_FLAG_OUT_FP32 = 2
 MLA_FLAG_VALIDATE = 4
+MLA_FLAG_BF16_PV = 8
 
 # every symbol include/mla_decode.h declares: name -> (restype, argtypes)
 _c_int, _c_size, _vp, _i64, _f32, _uint = (ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p,
@@ -35,7 +36,7 @@ SIGNATURES = {
     "mla_default_num_units": (_c_int, [_c_int, ctypes.POINTER(_c_int)]),
     "mla_decode_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int]),
     "mla_decode_plan": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _vp, _c_size, _vp]),
-    "mla_decode_plan_host": (_c_int, [_vp, _c_int, _c_int, _c_int, _vp, _vp]),
+    "mla_decode_plan_host": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _vp, _vp]),
     "mla_decode": (_c_int, [_vp, _vp, _i64, _vp, _i64, _vp, _c_int, _c_int, _c_int, _f32, _vp, _c_int,
                             _uint, _c_int, _vp, _c_size, _vp, _vp, _vp]),
     "mla_combine": (_c_int, [_vp, _c_size, _c_int, _c_int, _c_int, _uint, _c_int, _vp, _vp, _vp]),
@@ -120,15 +121,15 @@ def mla_decode_plan(cache_lens, batch: int, s_q: int, topk: int, num_units: int,
         int(ws_bytes), _stream(stream)))
 
 
-def mla_decode_plan_host(cache_lens, topk: int, num_units: int):
+def mla_decode_plan_host(cache_lens, s_q: int, topk: int, num_units: int):
     """Host-side partition: returns (unit_meta [U,5], req_meta [B,4]) as numpy int32."""
     import numpy as np
     lens = np.ascontiguousarray(np.asarray(cache_lens, dtype=np.int32))
     B = lens.size
     um = np.zeros((num_units, 5), np.int32)
     rm = np.zeros((B, 4), np.int32)
-    rc = load().mla_decode_plan_host(lens.ctypes.data, B, int(topk), int(num_units), um.ctypes.data,
-                                     rm.ctypes.data)
+    rc = load().mla_decode_plan_host(lens.ctypes.data, B, int(s_q), int(topk), int(num_units),
+                                     um.ctypes.data, rm.ctypes.data)
     _check("mla_decode_plan_host", rc)
     return um, rm
 

@@ -18,8 +18,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libmla_decode.so")
-SOURCES = ["decode_kernel.cu", "aux_kernels.cu", "api.cu", "noalloc.cu"]
-HEADERS = ["common.cuh", "plan.cuh", "ptx.cuh"]
+SOURCES = ["decode_kernel.cu", "mtp_kernel.cu", "aux_kernels.cu", "api.cu", "noalloc.cu"]
+HEADERS = ["common.cuh", "kernel_common.cuh", "plan.cuh", "ptx.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -14,8 +14,8 @@
 #include "plan.cuh"
 
 namespace mla {
-__global__ void mla_plan_kernel(const int* lens, int B, int topk, int U, int* hdr, int* unit_meta,
-                                int* req_meta, int slots_cap);
+__global__ void mla_plan_kernel(const int* lens, int B, int topk, int tile_rows, int U, int* hdr,
+                                int* unit_meta, int* req_meta, int slots_cap);
 __global__ void mla_combine_kernel(const int* req_meta, const float* part_lse, const float* part_o,
                                    int s_q, int out_fp32, void* out, float* lse);
 __global__ void mla_validate_kernel(const int* lens, const int* bt, long long bt_stride,
@@ -27,6 +27,10 @@ cudaError_t decode_set_attrs();
 cudaError_t decode_max_clusters(int* n, int num_clusters_hint);
 cudaError_t decode_launch(bool sparse, int num_clusters, cudaStream_t stream, const DecodeParams& p,
                           const CUtensorMap& tm_q, const CUtensorMap& tm_kv);
+cudaError_t mtp_set_attrs();
+cudaError_t mtp_max_clusters(int* n, int num_clusters_hint);
+cudaError_t mtp_launch(bool bf16_pv, int num_clusters, cudaStream_t stream, const DecodeParams& p,
+                       const CUtensorMap& tm_q, const CUtensorMap& tm_kv);
 }  // namespace mla
 
 using namespace mla;
@@ -39,7 +43,8 @@ constexpr int kMaxUnits = 4096;
 struct DeviceState {
   std::once_flag once;
   int status = MLA_OK;
-  int max_clusters = 0;  // co-resident 2-CTA clusters of the decode kernel
+  int max_clusters = 0;      // co-resident 2-CTA clusters of the one-token kernel
+  int max_clusters_mtp = 0;  // co-resident 4-CTA clusters of the two-token kernel
 };
 DeviceState g_dev[kMaxDevices];
 
@@ -79,7 +84,7 @@ int device_state(DeviceState** out) {
       st.status = MLA_ERR_DEVICE;
       return;
     }
-    if (decode_set_attrs() != cudaSuccess) {
+    if (decode_set_attrs() != cudaSuccess || mtp_set_attrs() != cudaSuccess) {
       cudaGetLastError();
       st.status = MLA_ERR_CUDA;
       return;
@@ -92,6 +97,12 @@ int device_state(DeviceState** out) {
       n = sms / 2;  // one cluster per SM pair
     }
     st.max_clusters = n > 0 ? n : 1;
+    int n4 = 0;
+    if (mtp_max_clusters(&n4, sms / 4 > 0 ? sms / 4 : 1) != cudaSuccess || n4 <= 0) {
+      cudaGetLastError();
+      n4 = sms / 4;
+    }
+    st.max_clusters_mtp = n4 > 0 ? n4 : 1;
   });
   *out = &st;
   return st.status;
@@ -143,7 +154,10 @@ int mla_default_num_units(int s_q, int* err) {
     if (err) *err = MLA_ERR_UNSUPPORTED;
     return 0;
   }
-  const int u = st->max_clusters / s_q;
+  // s_q = 2: one unit is a 4-CTA cluster serving both tokens (dense), or two
+  // 2-CTA clusters, one per token (top-k); take what both can keep resident
+  int u = st->max_clusters / s_q;
+  if (s_q == 2 && st->max_clusters_mtp < u) u = st->max_clusters_mtp;
   return u > 0 ? (u < kMaxUnits ? u : kMaxUnits) : 1;
 }
 
@@ -168,18 +182,20 @@ int mla_decode_plan(const int32_t* cache_lens, int batch, int s_q, int topk, int
   if (ws_bytes < L.total) return MLA_ERR_WORKSPACE;
   char* ws = static_cast<char*>(workspace);
   mla_plan_kernel<<<1, 1024, 0, static_cast<cudaStream_t>(stream)>>>(
-      cache_lens, batch, topk, U, reinterpret_cast<int*>(ws + L.hdr), reinterpret_cast<int*>(ws + L.units),
-      reinterpret_cast<int*>(ws + L.reqs), L.slots);
+      cache_lens, batch, topk, plan_tile_rows(s_q, topk), U, reinterpret_cast<int*>(ws + L.hdr),
+      reinterpret_cast<int*>(ws + L.units), reinterpret_cast<int*>(ws + L.reqs), L.slots);
   return last_cuda_error();
 }
 
-int mla_decode_plan_host(const int32_t* lens, int batch, int topk, int num_units, int32_t* unit_meta,
+int mla_decode_plan_host(const int32_t* lens, int batch, int s_q, int topk, int num_units, int32_t* unit_meta,
                          int32_t* req_meta) {
   if (!lens || !unit_meta || !req_meta || batch < 1 || topk < 0 || num_units < 1 || num_units > kMaxUnits)
     return MLA_ERR_INVALID_ARG;
+  if (s_q < 1 || s_q > 2) return MLA_ERR_UNSUPPORTED;
+  const int tile_rows = plan_tile_rows(s_q, topk);
   int total = 0;
   for (int b = 0; b < batch; ++b) {
-    const int n = plan_tiles(lens[b] > 0 ? lens[b] : 0, topk);
+    const int n = plan_tiles(lens[b] > 0 ? lens[b] : 0, topk, tile_rows);
     req_meta[4 * b + 0] = n;
     req_meta[4 * b + 3] = total;
     total += plan_cost(n);
@@ -208,7 +224,7 @@ int mla_decode(const void* q, const void* kv_cache, int64_t num_pages, const int
   if (!q || !kv_cache || !block_table || !cache_lens || !workspace || !out || !lse) return MLA_ERR_INVALID_ARG;
   if (batch < 1 || num_pages < 1 || bt_stride < 1 || topk < 0) return MLA_ERR_INVALID_ARG;
   if ((topk_idx == nullptr) != (topk == 0)) return MLA_ERR_INVALID_ARG;
-  if (flags & ~static_cast<unsigned>(MLA_FLAG_CAUSAL | MLA_FLAG_OUT_FP32 | MLA_FLAG_VALIDATE))
+  if (flags & ~static_cast<unsigned>(MLA_FLAG_CAUSAL | MLA_FLAG_OUT_FP32 | MLA_FLAG_VALIDATE | MLA_FLAG_BF16_PV))
     return MLA_ERR_INVALID_ARG;
   if (num_heads != kHeads || s_q < 1 || s_q > 2) return MLA_ERR_UNSUPPORTED;
   if (!std::isfinite(softmax_scale) || !(softmax_scale > 0.f)) return MLA_ERR_INVALID_ARG;
@@ -264,11 +280,19 @@ int mla_decode(const void* q, const void* kv_cache, int64_t num_pages, const int
   p.part_lse = reinterpret_cast<float*>(ws + L.part_lse);
   p.part_o = reinterpret_cast<float*>(ws + L.part_o);
 
+  // the two-token kernel moves Q through its 8 KiB chunk slots: 64-row boxes
+  const bool pair_path = plan_tile_rows(s_q, topk) == 128;
   CUtensorMap tm_q, tm_kv;
-  if ((rc = encode_2d(&tm_q, q, static_cast<uint64_t>(batch) * s_q * kHeads, kHeads)) != MLA_OK) return rc;
+  if ((rc = encode_2d(&tm_q, q, static_cast<uint64_t>(batch) * s_q * kHeads, pair_path ? kPage : kHeads)) !=
+      MLA_OK)
+    return rc;
   if ((rc = encode_2d(&tm_kv, kv_cache, static_cast<uint64_t>(num_pages) * kPage, kPage)) != MLA_OK) return rc;
 
-  const cudaError_t e = decode_launch(topk_idx != nullptr, U * s_q, s, p, tm_q, tm_kv);
+  // two query tokens, dense: both tokens share every tile (4-CTA clusters,
+  // paired-SM MMAs); otherwise one 2-CTA cluster per (unit, token)
+  const cudaError_t e = pair_path
+                            ? mtp_launch((flags & MLA_FLAG_BF16_PV) != 0, U, s, p, tm_q, tm_kv)
+                            : decode_launch(topk_idx != nullptr, U * s_q, s, p, tm_q, tm_kv);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return MLA_ERR_CUDA;
@@ -279,6 +303,8 @@ int mla_decode(const void* q, const void* kv_cache, int64_t num_pages, const int
 int mla_combine(void* workspace, size_t ws_bytes, int batch, int s_q, int num_heads, unsigned flags,
                 int num_units, void* out, float* lse, mla_stream_t stream) {
   if (!workspace || !out || !lse || batch < 1) return MLA_ERR_INVALID_ARG;
+  if (flags & ~static_cast<unsigned>(MLA_FLAG_CAUSAL | MLA_FLAG_OUT_FP32 | MLA_FLAG_VALIDATE | MLA_FLAG_BF16_PV))
+    return MLA_ERR_INVALID_ARG;
   if (num_heads != kHeads || s_q < 1 || s_q > 2) return MLA_ERR_UNSUPPORTED;
   if (!aligned(out, 16) || !aligned(lse, 4) || !aligned(workspace, 256)) return MLA_ERR_INVALID_ARG;
   DeviceState* st = nullptr;

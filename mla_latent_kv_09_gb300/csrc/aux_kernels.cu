@@ -40,13 +40,13 @@ __device__ int block_inclusive_scan(int v, int* s_warp, int& total) {
 // Step 2: split count and first partial slot per request.  Step 3: the
 // (request, tile) range of every unit.  Also resets the status word.
 __global__ void __launch_bounds__(1024) mla_plan_kernel(const int* __restrict__ lens, int B, int topk,
-                                                        int U, int* hdr, int* unit_meta, int* req_meta,
-                                                        int slots_cap) {
+                                                        int tile_rows, int U, int* hdr, int* unit_meta,
+                                                        int* req_meta, int slots_cap) {
   __shared__ int s_warp[32];
   int carry = 0, tot = 0;
   for (int base = 0; base < B; base += blockDim.x) {
     const int b = base + threadIdx.x;
-    const int n = b < B ? plan_tiles(max(lens[b], 0), topk) : 0;
+    const int n = b < B ? plan_tiles(max(lens[b], 0), topk, tile_rows) : 0;
     const int c = plan_cost(n);
     const int incl = block_inclusive_scan(c, s_warp, tot);
     if (b < B) {

@@ -39,6 +39,7 @@
 #include <cuda_runtime.h>
 
 #include "common.cuh"
+#include "kernel_common.cuh"
 #include "plan.cuh"
 #include "ptx.cuh"
 
@@ -75,8 +76,6 @@ constexpr uint32_t kColO = 0;     // O side: O, 512 columns
 constexpr int kThreads = 384;       // 12 warps
 constexpr int kConvThreads = 192;   // O side, dense: warps 4-7 and 10-11 convert V
 constexpr float kRescaleLog2 = 8.0f;
-constexpr uint64_t kTimeoutNs = 2000000000ull;
-constexpr uint64_t kDrainNs = 20000000ull;
 
 enum Bar {
   kKF = 0,        // [3] tile landed (TMA tx, or 128 gather arrivals)
@@ -103,39 +102,6 @@ constexpr uint32_t kIdescQK = idesc_bf16(128, 64, 0);
 constexpr uint32_t kIdescPV = (1u << 4) | (0u << 7) | (0u << 10) | (1u << 16) | ((256u >> 3) << 17) |
                               ((128u >> 4) << 24);
 
-struct Seg {
-  int b, t0, t1, n_tiles, slot;  // slot < 0: write the final output
-};
-
-// Walks the (request, tile-range) segments of one unit, in order.
-struct SegIter {
-  const int* req_meta;
-  int B, b, begin_b, begin_t, end_b, end_t, first_split;
-  __device__ SegIter(const DecodeParams& p, int unit) {
-    const int* um = p.unit_meta + 5 * unit;
-    req_meta = p.req_meta;
-    B = p.batch;
-    begin_b = um[0]; begin_t = um[1]; end_b = um[2]; end_t = um[3]; first_split = um[4];
-    b = begin_b;
-  }
-  __device__ bool next(Seg& s) {
-    while (b < B) {
-      if (b > end_b || (b == end_b && end_t == 0)) return false;
-      const int nt = req_meta[4 * b + 0];
-      const int ns = req_meta[4 * b + 1];
-      const int slot0 = req_meta[4 * b + 2];
-      const int t0 = (b == begin_b) ? begin_t : 0;
-      const int t1 = (b == end_b) ? end_t : nt;
-      const int split = (b == begin_b) ? first_split : 0;
-      s.b = b; s.t0 = t0; s.t1 = t1; s.n_tiles = nt;
-      s.slot = (ns > 1) ? slot0 + split : -1;
-      ++b;
-      if (t0 < t1) return true;
-    }
-    return false;
-  }
-};
-
 // Position in the 3-deep tile ring.
 struct Ring3 {
   uint32_t idx = 0, phase = 0;
@@ -143,50 +109,6 @@ struct Ring3 {
     if (++idx == kStages) { idx = 0; phase ^= 1u; }
   }
 };
-
-struct Ctl {
-  volatile uint32_t* abort;  // this CTA's abort flag (set by either CTA)
-  uint32_t abort_remote;     // the peer's abort flag (cluster address)
-  int* status;
-};
-
-__device__ __noinline__ void raise_timeout(const Ctl& c) {
-  *c.abort = 1u;
-  st_cluster_u32(c.abort_remote, 1u);
-  atomicCAS(c.status, 0, static_cast<int>(kStTimeout));
-}
-
-// Bounded wait: false if the wait ran out or the CTA pair is aborting.
-template <bool kCluster>
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ctl& c) {
-  if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  while (true) {
-    for (int i = 0; i < 16; ++i)
-      if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
-    if (*c.abort) return false;
-    if (globaltimer_ns() - t0 > kTimeoutNs) {
-      raise_timeout(c);
-      return false;
-    }
-  }
-}
-
-// Wait used only while tearing down after an abort: no abort check, short limit.
-__device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity) {
-  const uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer_ns() - t0 > kDrainNs) return;
-  }
-}
-
-__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const Ctl& c) {
-  return __all_sync(0xffffffffu, wait_bar<false>(bar, parity, c));
-}
 
 // tcgen05.mma with the A operand in tensor memory.
 __device__ __forceinline__ void umma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
@@ -202,30 +124,6 @@ __device__ __forceinline__ void umma_commit_multicast(uint32_t bar, uint16_t mas
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
       " [%0], %1;" ::"r"(bar), "h"(mask) : "memory");
-}
-
-// Remote shared-memory stores that complete on the destination CTA's mbarrier.
-__device__ __forceinline__ void st_async_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
-                                            uint32_t bar) {
-  asm volatile(
-      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];"
-      ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d), "r"(bar) : "memory");
-}
-__device__ __forceinline__ void st_async_b32(uint32_t addr, uint32_t v, uint32_t bar) {
-  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];"
-               ::"r"(addr), "r"(v), "r"(bar) : "memory");
-}
-
-__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
-  uint32_t r;
-  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-
-// bf16x2 word -> fp16x2 word (exact for |v| in [2^-14, 65504]; smaller values
-// become fp16 subnormals, absolute error <= 2^-25; larger ones overflow).
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
-  return pack_f16x2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
 }
 
 // Bytes of one P message (fp16 P tile, per-row rescale, and at the end of a
@@ -309,7 +207,8 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
 
   Ctl ctl;
   ctl.abort = &misc[1];
-  ctl.abort_remote = mapa(smem_u32(&misc[1]), peer);
+  ctl.abort_remote[0] = mapa(smem_u32(&misc[1]), peer);
+  ctl.n_remote = 1;
   ctl.status = p.ws_hdr + kHdrStatus;
   const float NEG_INF = -__int_as_float(0x7f800000);
 

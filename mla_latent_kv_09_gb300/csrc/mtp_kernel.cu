@@ -1,0 +1,855 @@
+// mtp_kernel.cu — MLA decode for requests with two query tokens (s_q = 2,
+// the multi-token-prediction step) on sm_103a, with paired-SM tensor-core
+// operations.
+//
+// What it computes is the attention of decode_kernel.cu ("DeepSeek V3/R1
+// Inference Efficiency (2)", §2.4.1, "MLA/MQA attention"); under the causal
+// mask the second token sees one more cached position than the first.  Both
+// tokens of a request read the same pages, so one tile of cached rows serves
+// both, and their 2 x 128 query heads form one M = 256 operand of a tcgen05
+// operation spread over a pair of SMs (cta_group::2: each SM of the pair holds
+// half of the rows of A and D and half of the columns of B).
+//
+// One work unit = one 4-CTA cluster = two SM pairs.  A tile is 128 cached
+// rows (two pages).
+//   Ranks 0, 1 (score pair).  Rank r holds token r's Q — dims 0..511 in
+//     tensor memory, the 64 RoPE dims in shared memory — and streams page r
+//     of every tile (all 576 dims) through a ring of 8 KiB chunk slots; Q
+//     dims 0..511 come through the same ring (and tcgen05.cp), the RoPE part
+//     into one of two alternating shared buffers.  Rank 0 issues S = Q K^T for both tokens
+//     (M = 256, N = 128, K = 576) into two alternating 128-column score
+//     buffers; token r's rows land in rank r.  Each rank runs the online
+//     softmax of its token (fp32, exp2 domain, lazy rescale: the reference max
+//     moves only when a score beats it by more than 2^8) and sends P plus the
+//     per-row rescale factor to rank 2 + r with st.async.
+//   Ranks 2, 3 (value pair).  Rank 2 + r owns token r's O (128 x 512 fp32,
+//     all of its tensor memory).  Rank 2 + r loads the value dims
+//     [128 r, 128 r + 128) and [256 + 128 r, 256 + 128 r + 128) of both pages
+//     (the B columns it holds in the pair) through a ring of page slots,
+//     converts them to fp16 in place, and rank 2 issues O += P V (M = 256,
+//     N = 2 x 256, K = 128).
+// Loads are latency-bound (HBM latency under this load is about 1.5 us), so
+// both rings free and refill at fine grain: chunk slots in groups of three as
+// soon as the score MMAs reading them finish, a page slot as soon as the value
+// MMAs of that page finish.  The MMA thread waits once per slot group: a wait
+// costs about 170 cycles of issue time, which a group's 12 queued MMAs hide.
+// P and V are fp16 (11 significant bits on the softmax weights; values must
+// stay below 65504 in magnitude), or bf16 in the kBf16PV variant.
+//
+// Warps (608 threads).  Score ranks: 0-15 softmax (warp w: head rows
+// 32 (w % 4) .., key columns 32 (w / 4) .. of each tile), 16 MMA issue on rank
+// 0 and tensor-memory owner, 17 TMA producer, 18 P shipper.  Value ranks: 0-3
+// O rescale and epilogue (thread i = head row i), 4-15 V conversion, 16 MMA
+// issue on rank 2 and tensor-memory owner, 17 TMA producer.
+//
+// P travels as one bulk copy per tile: the softmax warps write it into a
+// local copy laid out as the value rank's A operand; the shipper warp sends
+// it with cp.async.bulk (completing on the value rank's barrier) once PV is
+// done with the destination slot, and frees the local copy when the bulk copy
+// has read it.  Shared-memory-to-shared-memory traffic between SMs is the
+// narrowest path of this kernel (about 21 B per clock per SM), so the softmax
+// warps never wait for it except when they are a whole tile ahead.
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "kernel_common.cuh"
+#include "plan.cuh"
+#include "ptx.cuh"
+
+namespace mla {
+namespace mtp {
+
+constexpr int kTileRows = 2 * kPage;              // 128 cached rows per tile
+constexpr int kPageChunk = kPage * 128;           // 8 KiB: 64 rows x 64 dims (bf16), 128B-swizzled
+constexpr int kKSlots = 18;                       // score ranks: chunk slots (two pages)
+constexpr int kKGroup = 3;                        // chunk slots per landing / free barrier
+constexpr int kKGroups = kKSlots / kKGroup;
+constexpr int kVPage = 4 * kPageChunk;            // 32 KiB: one page, this rank's 256 value dims
+constexpr int kVSlots = 4;                        // value ranks: page slots (two tiles)
+// P tile, 128 heads x 128 keys of 16-bit weights, as a K-major 128B-swizzled
+// operand whose 8-row groups hold both 64-key halves side by side: byte
+// (row / 8) * 2048 + half * 1024 + (row % 8) * 128 + swizzled 16-B piece.  A
+// row quarter (32 rows) is then one contiguous 8 KiB block.
+constexpr int kPSlot = kHeads * 256;              // 32 KiB
+constexpr int kPGroupStride = 2048;               // between 8-row groups
+constexpr int kPHalfStride = 1024;                // between the two 64-key halves
+constexpr int kQChunk = kHeads * 128;             // 16 KiB: 128 heads x 64 dims (bf16)
+
+// Shared memory (offsets from a 1024-aligned base; the barrier block sits at
+// the same offset in all four CTAs, which multicast commits rely on).
+constexpr int kOffStage = 0;                         // chunk slots (score ranks) / page slots (value ranks)
+constexpr int kOffQr = kKSlots * kPageChunk;         // score ranks: [2] Q dims 512..575
+constexpr int kOffXchg = kOffQr + 2 * kQChunk;       // score ranks: row max / sum exchange, 6 KiB
+constexpr int kOffPs = kOffXchg + 6144;              // score ranks: outgoing P tile (same layout as kOffP)
+constexpr int kOffAlphaS = kOffPs + kPSlot;          // score ranks: outgoing float[128] rescale factors
+constexpr int kOffFinS = kOffAlphaS + kHeads * 4;    // score ranks: outgoing float[128] final scales
+constexpr int kEndS = kOffFinS + kHeads * 4;         // 201728
+constexpr int kOffP = kVSlots * kVPage;              // value ranks: [2] P tiles
+constexpr int kOffAlpha = kOffP + 2 * kPSlot;        // value ranks: float[2][128]
+constexpr int kOffFin = kOffAlpha + 2 * kHeads * 4;  // value ranks: float[2][128]
+constexpr int kEndO = kOffFin + 2 * kHeads * 4;      // 198656
+constexpr int kOffBar = kEndS > kEndO ? kEndS : kEndO;
+constexpr int kBarBytes = 640;
+constexpr int kAlignSlack = 1024;
+constexpr int kSmemBytes = kOffBar + kBarBytes + kAlignSlack;
+static_assert(kOffPs % 1024 == 0 && kOffP % 1024 == 0, "P tiles keep the 128-byte swizzle phase");
+static_assert(kSmemBytes <= 232448, "shared memory");
+
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0;    // score ranks: two 128-column score buffers
+constexpr uint32_t kColQ = 256;  // score ranks: Q dims 0..511, 8 chunks of 32 columns
+constexpr uint32_t kColO = 0;    // value ranks: O, 512 columns
+
+constexpr int kThreads = 608;                    // 19 warps
+constexpr int kSoftmaxWarps = 16;
+constexpr int kConvThreads = 384;                // value ranks: warps 4-15
+constexpr int kMmaWarp = 16;
+constexpr int kTmaWarp = 17;
+constexpr int kShipWarp = 18;                    // score ranks: P shipper
+constexpr float kRescaleLog2 = 8.0f;
+
+constexpr uint16_t kScoreMask = 0x3;  // ranks 0, 1
+constexpr uint16_t kValueMask = 0xC;  // ranks 2, 3
+
+enum Bar {
+  kKF = 0,        // [6] rank 0: slot group landed in both score ranks (3 arrivals + TMA tx of both)
+  kKE = 6,        // [6] score ranks: slot group free (commit from rank 0)
+  kQRF = 12,      // [2] rank 0: Q RoPE buffer landed in both score ranks (TMA tx of both)
+  kQFree = 14,    // [2] score ranks: the score MMAs of the segment using that RoPE buffer finished
+  kQF = 36,       // score ranks: a segment's last score MMA finished (Q may be replaced)
+  kQR = 37,       // (unused)
+  kSF = 38,       // [2] score ranks: scores ready (commit from rank 0)
+  kSE = 40,       // [2] rank 0: scores read (one arrival per row quarter of both ranks)
+  kPFree = 42,    // [2] score ranks: PV finished with that P slot (commit from rank 2)
+  kVF = 44,       // [4] value ranks: page slot landed (TMA tx)
+  kVE = 48,       // [4] value ranks: page slot free (commit from rank 2)
+  kVR = 52,       // [4] rank 2: page slot converted in both value ranks
+  kPM = 56,       // [2] value ranks: P message landed (1 arrival + tx bytes)
+  kPR = 58,       // [2] rank 2: O rescaled and P landed in both value ranks
+  kPD = 60,       // [2] value ranks: PV of a tile of that parity finished (commit from rank 2)
+  kOF = 62,       // value ranks: a segment's last PV finished (commit from rank 2)
+  kOE = 63,       // rank 2: both value ranks' epilogues read O
+  kMmaDone = 64,  // teardown
+  kPsFull = 65,   // score ranks: the local P copy is written (one arrival per softmax warp)
+  kPsFree = 66,   // score ranks: the bulk copy has read the local P copy
+  kNumBars = 67
+};
+static_assert(kNumBars * 8 + 16 <= kBarBytes, "barrier block");
+
+// kind::f16 instruction descriptors.  Scores: bf16 operands, M = 256, N = 128,
+// B (the cached rows) K-major.  Values: fp16 or bf16 operands (A and B of
+// one MMA always share a type), M = 256, N = 256, B (V) MN-major.
+constexpr uint32_t kIdescQK = idesc_bf16(256, 128, 0);
+template <bool kBf16PV>
+__host__ __device__ constexpr uint32_t idesc_pv() {
+  return (1u << 4) | ((kBf16PV ? 1u : 0u) << 7) | ((kBf16PV ? 1u : 0u) << 10) | (1u << 16) |
+         ((256u >> 3) << 17) | ((256u >> 4) << 24);
+}
+
+// Position in an N-slot ring.
+template <uint32_t N>
+struct Ring {
+  uint32_t idx = 0, phase = 0;
+  __device__ void advance() {
+    if (++idx == N) {
+      idx = 0;
+      phase ^= 1u;
+    }
+  }
+};
+
+// Bytes of one P message: the 16-bit P tile, the per-row rescale factor and,
+// at the end of a segment, the per-row final scale.
+__host__ __device__ constexpr uint32_t p_message_bytes(bool last) {
+  return static_cast<uint32_t>(kPSlot + kHeads * 4 + (last ? kHeads * 4 : 0));
+}
+
+template <bool kBf16PV>
+__global__ void __launch_bounds__(kThreads, 1)
+mla_decode_mtp_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tm_q,
+                      const __grid_constant__ CUtensorMap tm_kv) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t mis = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+  uint8_t* smem = smem_raw + mis;
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t rank = cluster_ctarank();  // 0, 1: score pair; 2, 3: value pair
+  const uint32_t tok = rank & 1u;           // the query token this CTA serves
+  const bool score_rank = rank < 2;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int unit = blockIdx.x >> 2;
+
+  {  // a unit with no work leaves at once (all four CTAs see the same range)
+    const int* um = p.unit_meta + 5 * unit;
+    if (um[0] >= p.batch || (um[0] == um[2] && um[1] >= um[3])) return;
+  }
+  if (mis > kAlignSlack) {  // never touch shared memory past the end of the allocation
+    if (threadIdx.x == 0) atomicCAS(p.ws_hdr + kHdrStatus, 0, static_cast<int>(kStWorkspace));
+    return;
+  }
+
+  auto kslot = [&](uint32_t i) -> uint32_t { return sbase + kOffStage + i * static_cast<uint32_t>(kPageChunk); };
+  auto vslot = [&](uint32_t i) -> uint32_t { return sbase + kOffStage + i * static_cast<uint32_t>(kVPage); };
+  auto bar = [&](int i) -> uint32_t { return sbase + kOffBar + 8u * static_cast<uint32_t>(i); };
+  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + kOffBar + 8 * kNumBars);
+  // misc[0] = tensor-memory base, misc[1] = abort flag
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kKGroups; ++i) {
+      mbar_init(bar(kKF + i), kKGroup);
+      mbar_init(bar(kKE + i), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(kQRF + i), 1);
+      mbar_init(bar(kQFree + i), 1);
+    }
+    for (int i = 0; i < kVSlots; ++i) {
+      mbar_init(bar(kVF + i), 1);
+      mbar_init(bar(kVE + i), 1);
+      mbar_init(bar(kVR + i), 2);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(kSF + i), 1);
+      mbar_init(bar(kSE + i), 8);
+      mbar_init(bar(kPFree + i), 1);
+      mbar_init(bar(kPM + i), 1);
+      mbar_init(bar(kPR + i), 2);
+      mbar_init(bar(kPD + i), 1);
+    }
+    mbar_init(bar(kQF), 1);
+    mbar_init(bar(kOF), 1);
+    mbar_init(bar(kOE), 2);
+    mbar_init(bar(kMmaDone), 1);
+    mbar_init(bar(kPsFull), kSoftmaxWarps);
+    mbar_init(bar(kPsFree), 1);
+    misc[1] = 0u;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc_pair(smem_u32(&misc[0]), kTmemCols);
+    tmem_relinquish_pair();
+  }
+  if (warp == kTmaWarp && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_kv);
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // every CTA's barriers exist before any remote operation
+  tc_fence_after();
+  const uint32_t tmem = misc[0];
+
+  Ctl ctl;
+  ctl.abort = &misc[1];
+  ctl.n_remote = 0;
+  for (uint32_t r = 0; r < 4; ++r)
+    if (r != rank) ctl.abort_remote[ctl.n_remote++] = mapa(smem_u32(&misc[1]), r);
+  ctl.status = p.ws_hdr + kHdrStatus;
+  const float NEG_INF = -__int_as_float(0x7f800000);
+  const int U = p.num_units;
+
+  if (score_rank && warp < kSoftmaxWarps) {
+    // ================================================= softmax (score ranks)
+    // Warp (q4, cg): head rows 32 q4 .. +31 (its tensor-memory lane quarter),
+    // key columns 32 cg .. +31 of the tile.  The four warps of a quarter
+    // combine their row maxima through shared memory (named barrier 1 + q4).
+    const int q4 = warp & 3, cg = warp >> 2;
+    const int row = q4 * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
+    const bool lead = cg == 0;  // the quarter's leading warp signals and writes the row scales
+    // this thread's four 16-B pieces: half cg / 2 of the keys, pieces 4 (cg % 2) ..
+    const uint32_t sProw = sbase + kOffPs + static_cast<uint32_t>(row >> 3) * kPGroupStride +
+                           static_cast<uint32_t>(cg >> 1) * kPHalfStride + static_cast<uint32_t>(row & 7) * 128u;
+    const uint32_t piece0 = static_cast<uint32_t>(cg & 1) * 4u;
+    float* alpha_out = reinterpret_cast<float*>(smem + kOffAlphaS);
+    float* fin_out = reinterpret_cast<float*>(smem + kOffFinS);
+    const uint32_t rSE = mapa(bar(kSE), 0);
+    float* xmax = reinterpret_cast<float*>(smem + kOffXchg);                   // [2 parity][4 cg][128]
+    float* xsum = reinterpret_cast<float*>(smem + kOffXchg + 8 * kHeads * 4);  // [4 cg][128]
+    const int qbar = 1 + q4;
+    SegIter it(p, unit);
+    Seg sg;
+    uint32_t g = 0;
+    bool ok = true, stop = false;  // ok: this warp's waits so far; stop: the quarter leaves
+    while (!stop && it.next(sg)) {
+      const int L = max(p.cache_lens[sg.b], 0);
+      const int vis = p.causal ? L - 1 + static_cast<int>(tok) : L;
+      const long long bt_row = static_cast<long long>(sg.b) * 2 + tok;
+      // z: sum of the fp32 weights; it normalises O and gives the LSE (O then
+      // carries the weights' 16-bit rounding once more, relative <= 2^-11 for
+      // fp16 and 2^-9 for bf16)
+      float m_used = NEG_INF, z = 0.f;
+      for (int j = sg.t0; j < sg.t1; ++j, ++g) {
+        const uint32_t sb = g & 1u, ph = (g >> 1) & 1u;
+        const bool last = (j == sg.t1 - 1);
+        ok = ok && warp_wait(bar(kSF + sb), ph, ctl);
+        float s[32];
+        if (ok) {
+          tc_fence_after();
+          uint32_t r[32];
+          tmem_ld32(tmem + lane_base + kColS + 128u * sb + 32u * cg, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) s[c] = __uint_as_float(r[c]);
+          tc_fence_before();
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) s[c] = NEG_INF;
+        }
+
+        // ---- causal / length mask, then the row max over the quarter's warps
+        const int nvalid = vis - (j * kTileRows + 32 * cg);
+        if (nvalid < 32) {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) s[c] = c < nvalid ? s[c] : NEG_INF;
+        }
+        {
+          float m4[4] = {NEG_INF, NEG_INF, NEG_INF, NEG_INF};
+#pragma unroll
+          for (int c = 0; c < 32; ++c) m4[c & 3] = fmaxf(m4[c & 3], s[c]);
+          xmax[(sb * 4 + cg) * kHeads + row] = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+        }
+        if (!named_bar_all(qbar, 128, ok)) {
+          stop = true;
+          break;
+        }
+        if (lead && lane == 0) mbar_arrive_remote(rSE + 8u * sb);  // the quarter has read its scores
+        const float* xm = xmax + sb * 4 * kHeads + row;
+        const float mt = fmaxf(fmaxf(xm[0], xm[kHeads]), fmaxf(xm[2 * kHeads], xm[3 * kHeads])) * p.scale_log2;
+
+        float alpha = 1.f;
+        if (mt > m_used + kRescaleLog2) {
+          alpha = (m_used == NEG_INF) ? 0.f : ex2_approx(m_used - mt);
+          m_used = mt;
+          z *= alpha;
+        }
+        uint32_t pk[16];
+        if (m_used == NEG_INF) {
+#pragma unroll
+          for (int c = 0; c < 16; ++c) pk[c] = 0u;
+        } else {
+          float ze[4] = {0.f, 0.f, 0.f, 0.f};
+          const float nm = -m_used;
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const float p0 = ex2_approx(fmaf(s[2 * c], p.scale_log2, nm));
+            const float p1 = ex2_approx(fmaf(s[2 * c + 1], p.scale_log2, nm));
+            pk[c] = kBf16PV ? pack_bf16x2(p0, p1) : pack_f16x2(p0, p1);
+            ze[c & 3] += p0 + p1;
+          }
+          z += (ze[0] + ze[1]) + (ze[2] + ze[3]);
+        }
+        // ---- the local P copy: free once the previous tile's bulk copy read it
+        if (g > 0) ok = ok && warp_wait(bar(kPsFree), (g - 1u) & 1u, ctl);
+        if (ok) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            st_shared_v4(sProw + (((piece0 + static_cast<uint32_t>(k)) ^ (row & 7)) << 4), pk[4 * k],
+                         pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+          if (lead) alpha_out[row] = alpha;
+        }
+        if (last) {  // ---- segment end: the quarter's partial sums -> final scale and LSE
+          xsum[cg * kHeads + row] = z;
+          if (!named_bar_all(qbar, 128, ok)) {
+            stop = true;
+            break;
+          }
+          if (lead) {
+            const float zt = (z + xsum[kHeads + row]) + (xsum[2 * kHeads + row] + xsum[3 * kHeads + row]);
+            fin_out[row] = zt > 0.f ? 1.f / zt : 0.f;  // O_final = O_acc / z
+            const float lse = zt > 0.f ? (m_used + log2f(zt)) * 0.69314718055994531f : NEG_INF;
+            if (sg.slot < 0) {
+              p.lse[bt_row * kHeads + row] = lse;
+            } else if (sg.slot < 2 * U) {  // the plan never uses more than 2 * (U - 1) slots
+              p.part_lse[(static_cast<long long>(sg.slot) * 2 + tok) * kHeads + row] = lse;
+            }
+          }
+        }
+        if (ok) {
+          fence_proxy_async_smem();  // generic writes above, read next by the bulk copy
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(kPsFull));
+        }
+      }
+    }
+  } else if (score_rank && warp == kShipWarp) {
+    // ================================================= P shipper (score ranks, one lane)
+    if (lane == 0) {
+      const uint32_t vrank = 2u + tok;
+      const uint32_t rP = mapa(sbase + kOffP, vrank);
+      const uint32_t rAlpha = mapa(sbase + kOffAlpha, vrank);
+      const uint32_t rFin = mapa(sbase + kOffFin, vrank);
+      const uint32_t rPM = mapa(bar(kPM), vrank);
+      SegIter it(p, unit);
+      Seg sg;
+      uint32_t g = 0;
+      bool ok = true;
+      while (ok && it.next(sg)) {
+        for (int j = sg.t0; j < sg.t1; ++j, ++g) {
+          const uint32_t sb = g & 1u, ph = (g >> 1) & 1u;
+          if (!(ok = wait_bar<false>(bar(kPsFull), g & 1u, ctl))) break;
+          if (!(ok = wait_bar<false>(bar(kPFree + sb), ph ^ 1u, ctl))) break;  // PV is done with that slot
+          const uint32_t mbar = rPM + 8u * sb;
+          bulk_copy_s2c(rP + sb * kPSlot, sbase + kOffPs, static_cast<uint32_t>(kPSlot), mbar);
+          bulk_copy_s2c(rAlpha + sb * kHeads * 4u, sbase + kOffAlphaS, kHeads * 4u, mbar);
+          if (j == sg.t1 - 1) bulk_copy_s2c(rFin + sb * kHeads * 4u, sbase + kOffFinS, kHeads * 4u, mbar);
+          bulk_commit();
+          bulk_wait_read();
+          mbar_arrive(bar(kPsFree));
+        }
+      }
+      bulk_wait_all();  // copies out of this CTA's memory are complete
+    }
+    __syncwarp();
+  } else if (!score_rank && warp < 4) {
+    // ================================================= O rescale + epilogue (value ranks)
+    const int row = threadIdx.x;
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const volatile float* alpha_s = reinterpret_cast<const volatile float*>(smem + kOffAlpha);
+    const volatile float* fin_s = reinterpret_cast<const volatile float*>(smem + kOffFin);
+    const uint32_t rPR = mapa(bar(kPR), 2);
+    const uint32_t rOE = mapa(bar(kOE), 2);
+    SegIter it(p, unit);
+    Seg sg;
+    uint32_t g = 0, nseg = 0;
+    bool ok = true, stop = false;  // the four warps vote at every named barrier
+    while (!stop && it.next(sg)) {
+      float fin = 0.f;
+      for (int j = sg.t0; j < sg.t1; ++j, ++g) {
+        const uint32_t pb = g & 1u, ph = (g >> 1) & 1u;
+        const bool last = (j == sg.t1 - 1);
+        if (row == 0) mbar_arrive_expect_tx(bar(kPM + pb), p_message_bytes(last));
+        ok = ok && warp_wait<true>(bar(kPM + pb), ph, ctl);
+        const float alpha = ok ? alpha_s[pb * kHeads + row] : 1.f;
+        if (last && ok) fin = fin_s[pb * kHeads + row];
+        const bool resc = ok && (j != sg.t0) && alpha != 1.f;
+        if (__any_sync(0xffffffffu, resc)) {  // tcgen05.ld/st are warp-collective
+          // PV(g-1) finished: phase (g-1)/2 of the barrier of its parity (the
+          // phase before it, PV(g-3), is known complete: P(g-1) was sent after it)
+          const uint32_t gp = g - 1u;
+          ok = warp_wait(bar(kPD + (gp & 1u)), (gp >> 1) & 1u, ctl);
+        }
+        if (__any_sync(0xffffffffu, resc) && ok) {
+          tc_fence_after();
+          const float a = resc ? alpha : 1.f;
+#pragma unroll 1
+          for (int cc = 0; cc < 16; ++cc) {
+            uint32_t r[32];
+            const uint32_t ta = tmem + lane_base + kColO + 32u * cc;
+            tmem_ld32(ta, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int c = 0; c < 32; ++c) r[c] = __float_as_uint(__uint_as_float(r[c]) * a);
+            tmem_st32(ta, r);
+          }
+          tmem_wait_st();
+        }
+        fence_proxy_async_smem();  // P written by the bulk copy, read next by the tensor core
+        tc_fence_before();
+        if (!named_bar_all(5, 128, ok)) {
+          stop = true;
+          break;
+        }
+        if (row == 0) mbar_arrive_remote(rPR + 8u * pb);
+
+        if (last) {  // ---- segment epilogue: O * fin -> global
+          ok = warp_wait(bar(kOF), nseg & 1u, ctl);
+          if (!named_bar_all(5, 128, ok)) {
+            stop = true;
+            break;
+          }
+          tc_fence_after();
+          const long long bt_row = static_cast<long long>(sg.b) * 2 + tok;
+          if (sg.slot < 0 && !p.out_fp32) {
+            uint16_t* dst0 = static_cast<uint16_t*>(p.out) + (bt_row * kHeads + row) * kDv;
+#pragma unroll 1
+            for (int cc = 0; cc < 16; ++cc) {
+              uint32_t r[32];
+              tmem_ld32(tmem + lane_base + kColO + 32u * cc, r);
+              tmem_wait_ld();
+              uint4* dst = reinterpret_cast<uint4*>(dst0 + 32 * cc);
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                dst[k] = make_uint4(
+                    pack_bf16x2(__uint_as_float(r[8 * k + 0]) * fin, __uint_as_float(r[8 * k + 1]) * fin),
+                    pack_bf16x2(__uint_as_float(r[8 * k + 2]) * fin, __uint_as_float(r[8 * k + 3]) * fin),
+                    pack_bf16x2(__uint_as_float(r[8 * k + 4]) * fin, __uint_as_float(r[8 * k + 5]) * fin),
+                    pack_bf16x2(__uint_as_float(r[8 * k + 6]) * fin, __uint_as_float(r[8 * k + 7]) * fin));
+            }
+          } else if (sg.slot < 2 * U) {
+            float* dst0 = sg.slot < 0
+                ? static_cast<float*>(p.out) + (bt_row * kHeads + row) * kDv
+                : p.part_o + ((static_cast<long long>(sg.slot) * 2 + tok) * kHeads + row) * kDv;
+#pragma unroll 1
+            for (int cc = 0; cc < 16; ++cc) {
+              uint32_t r[32];
+              tmem_ld32(tmem + lane_base + kColO + 32u * cc, r);
+              tmem_wait_ld();
+              float4* dst = reinterpret_cast<float4*>(dst0 + 32 * cc);
+#pragma unroll
+              for (int k = 0; k < 8; ++k)
+                dst[k] = make_float4(__uint_as_float(r[4 * k]) * fin, __uint_as_float(r[4 * k + 1]) * fin,
+                                     __uint_as_float(r[4 * k + 2]) * fin, __uint_as_float(r[4 * k + 3]) * fin);
+            }
+          }
+          tc_fence_before();
+          named_bar_sync(5, 128);
+          if (row == 0) mbar_arrive_remote(rOE);
+        }
+      }
+      ++nseg;
+    }
+  } else if (warp == kMmaWarp) {
+    // ================================================= MMA issue (ranks 0 and 2, one thread)
+    if (lane == 0 && rank == 0) {
+      // The ring is consumed in "uses" of one 8 KiB slot: a K chunk (1 use),
+      // half of a Q chunk (1 use; a Q chunk is two adjacent slots) or a pad
+      // (1 use, keeps Q chunks on even slots).  Slot groups are waited for
+      // before their first use and freed after their last.  Plain counters
+      // (no captures): this loop must issue an MMA every ~64 cycles.
+      SegIter it(p, unit);
+      Seg sg;
+      uint32_t g = 0, nseg = 0;
+      uint32_t u = 0;       // uses consumed
+      uint32_t waited = 0;  // slot-group phases waited for
+      bool ok = true;
+      const uint32_t kf0 = bar(kKF), ke0 = bar(kKE), slot0 = sbase + kOffStage;
+      while (ok && it.next(sg)) {
+        // Q: the old one is free once the previous segment's score MMAs finish
+        if (nseg > 0 && !(ok = wait_bar<false>(bar(kQF), (nseg - 1u) & 1u, ctl))) break;
+        tc_fence_after();
+        const uint32_t u_q = u + (u & 1u);  // first Q use (after a pad)
+        for (int i = 0; i < 8 && ok; ++i) {
+          const uint32_t ue = u_q + 2u * i + 2u;  // uses [.., ue) must have landed
+          while (waited * kKGroup < ue) {
+            if (!(ok = wait_bar<true>(kf0 + 8u * (waited % kKGroups), (waited / kKGroups) & 1u, ctl))) break;
+            tc_fence_after();
+            ++waited;
+          }
+          if (!ok) break;
+          const uint32_t uq = u_q + 2u * i;
+          const uint64_t qd = smem_desc(slot0 + (uq % kKSlots) * kPageChunk, 16u, 1024u);  // two adjacent slots
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            tmem_cp_pair_128x256b(tmem + kColQ + 32u * i + 8u * kk, qd + static_cast<uint64_t>((32 * kk) >> 4));
+          // free the groups all of whose uses are now consumed
+          for (uint32_t f = u / kKGroup; (f + 1) * kKGroup <= ue; ++f)
+            umma_commit_pair(ke0 + 8u * (f % kKGroups), kScoreMask);
+          u = ue;
+        }
+        if (!ok) break;
+        if (!(ok = wait_bar<true>(bar(kQRF + (nseg & 1u)), (nseg >> 1) & 1u, ctl))) break;
+        const uint64_t qr0 = smem_desc(sbase + kOffQr + (nseg & 1u) * kQChunk, 16u, 1024u);
+        for (int j = sg.t0; j < sg.t1 && ok; ++j, ++g) {
+          const uint32_t sb = g & 1u, ph = (g >> 1) & 1u;
+          if (!(ok = wait_bar<true>(bar(kSE + sb), ph ^ 1u, ctl))) break;
+          tc_fence_after();
+          const uint32_t dS = tmem + kColS + 128u * sb;
+          // K = 576 in 36 steps of 16, one 64-dim chunk per slot
+#pragma unroll
+          for (int c = 0; c < kNumChunks; ++c) {
+            const uint32_t uc = u + c;
+            if (waited * kKGroup <= uc) {  // uc opens a new slot group
+              if (!(ok = wait_bar<true>(kf0 + 8u * (waited % kKGroups), (waited / kKGroups) & 1u, ctl))) break;
+              tc_fence_after();
+              ++waited;
+            }
+            const uint64_t bd = smem_desc(slot0 + (uc % kKSlots) * kPageChunk, 16u, 1024u);
+            if (c < 8) {
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                umma_pair_ta(dS, tmem + kColQ + 32u * c + 8u * kk, bd + static_cast<uint64_t>((32 * kk) >> 4),
+                             kIdescQK, (c | kk) != 0 ? 1u : 0u);
+            } else {
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                umma_pair_sa(dS, qr0 + static_cast<uint64_t>((32 * kk) >> 4),
+                             bd + static_cast<uint64_t>((32 * kk) >> 4), kIdescQK, 1u);
+            }
+            if ((uc + 1) % kKGroup == 0) umma_commit_pair(ke0 + 8u * ((uc / kKGroup) % kKGroups), kScoreMask);
+          }
+          if (!ok) break;
+          u += kNumChunks;
+          umma_commit_pair(bar(kSF + sb), kScoreMask);
+          if (j == sg.t1 - 1) {
+            umma_commit_pair(bar(kQF), kScoreMask);
+            umma_commit_pair(bar(kQFree + (nseg & 1u)), kScoreMask);
+          }
+        }
+        ++nseg;
+      }
+      umma_commit_pair(bar(kMmaDone), 1u << 0);  // every MMA issued so far has finished
+      drain_bar(bar(kMmaDone), 0);
+    } else if (lane == 0 && rank == 2) {
+      SegIter it(p, unit);
+      Seg sg;
+      Ring<kVSlots> rv;
+      uint32_t g = 0, nseg = 0;
+      bool ok = true;
+      constexpr uint32_t kIdescPV = idesc_pv<kBf16PV>();
+      while (ok && it.next(sg)) {
+        for (int j = sg.t0; j < sg.t1 && ok; ++j, ++g) {
+          const uint32_t pb = g & 1u, ph = (g >> 1) & 1u;
+          const bool first = (j == sg.t0);
+          if (!(ok = wait_bar<true>(bar(kPR + pb), ph, ctl))) break;
+          if (first && !(ok = wait_bar<true>(bar(kOE), (nseg & 1u) ^ 1u, ctl))) break;
+          const uint64_t ad0 = smem_desc(sbase + kOffP + pb * kPSlot, 16u, static_cast<uint32_t>(kPGroupStride));
+          // the tile's two pages, 64 keys each (K = 4 x 16 per page)
+#pragma unroll 1
+          for (int e = 0; e < 2; ++e, rv.advance()) {
+            if (!(ok = wait_bar<true>(bar(kVR + rv.idx), rv.phase, ctl))) break;
+            tc_fence_after();
+            const uint64_t bd0 = smem_desc(vslot(rv.idx), static_cast<uint32_t>(kPageChunk), 1024u);  // MN-major
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+#pragma unroll
+              for (int h = 0; h < 2; ++h)
+                umma_pair_sa(tmem + kColO + 256u * h,
+                             ad0 + static_cast<uint64_t>((e * kPHalfStride + kk * 32) >> 4),
+                             bd0 + static_cast<uint64_t>((h * 2 * kPageChunk + 2048 * kk) >> 4), kIdescPV,
+                             (first && e == 0 && kk == 0) ? 0u : 1u);
+            }
+            umma_commit_pair(bar(kVE + rv.idx), kValueMask);
+          }
+          if (!ok) break;
+          umma_commit_pair(bar(kPFree + pb), kScoreMask);  // the score ranks may reuse this P slot
+          umma_commit_pair(bar(kPD + pb), kValueMask);
+          if (j == sg.t1 - 1) umma_commit_pair(bar(kOF), kValueMask);
+        }
+        ++nseg;
+      }
+      umma_commit_pair(bar(kMmaDone), 1u << 2);
+      drain_bar(bar(kMmaDone), 0);
+    }
+    __syncwarp();
+  } else if (warp == kTmaWarp) {
+    // ================================================= TMA producers (whole warp; lane 0 issues)
+    // Page ids are read 32 tiles at a time with one coalesced load; a page
+    // past the cache end or outside the pool reads the TMA fill value (zeros).
+    SegIter it(p, unit);
+    Seg sg;
+    uint32_t issued = 0;
+    bool ok = true;
+    if (score_rank) {
+      // Both score ranks fill their own chunk slots; every copy completes on
+      // rank 0's barriers, which rank 0 arms with the bytes of both.  The use
+      // sequence is the MMA thread's: per segment a pad if needed, 16 Q
+      // halves, then 9 K chunks per tile.
+      const uint32_t rKF = mapa(bar(kKF), 0);
+      const uint32_t rQRF = mapa(bar(kQRF), 0);
+      uint32_t u = 0, nseg = 0;
+      // claim the next slot: wait for its group to be free at the group's first use
+      auto claim = [&](uint32_t bytes) -> bool {
+        const uint32_t sl = u % kKSlots, grp = sl / kKGroup;
+        if (sl % kKGroup == 0 && !warp_wait(bar(kKE + grp), ((u / kKSlots) & 1u) ^ 1u, ctl)) return false;
+        if (lane == 0 && tok == 0) mbar_arrive_expect_tx(bar(kKF + grp), 2u * bytes);
+        return true;
+      };
+      while (ok && it.next(sg)) {
+        const int L = max(p.cache_lens[sg.b], 0);
+        const int qy = (sg.b * 2 + static_cast<int>(tok)) * kHeads;
+        // RoPE part of Q into buffer nseg % 2 once segment nseg - 2 is done with it
+        if (nseg >= 2 && !(ok = warp_wait(bar(kQFree + (nseg & 1u)), ((nseg - 2u) >> 1) & 1u, ctl))) break;
+        if (lane == 0) {
+          if (tok == 0) mbar_arrive_expect_tx(bar(kQRF + (nseg & 1u)), 2u * kQChunk);
+          for (int h = 0; h < 2; ++h)
+            tma_load_2d_pair(sbase + kOffQr + (nseg & 1u) * kQChunk + h * kPageChunk, &tm_q, 8 * kChunk,
+                             qy + h * kPage, rQRF + 8u * (nseg & 1u));
+        }
+        if (u & 1u) {  // pad
+          if (!(ok = claim(0))) break;
+          ++u;
+        }
+        for (int i = 0; i < 8 && ok; ++i) {
+          for (int h = 0; h < 2; ++h) {
+            if (!(ok = claim(kPageChunk))) break;
+            if (lane == 0)
+              tma_load_2d_pair(kslot(u % kKSlots), &tm_q, i * kChunk, qy + h * kPage,
+                               rKF + 8u * ((u % kKSlots) / kKGroup));
+            ++u;
+          }
+        }
+        if (!ok) break;
+        const int* bt_row = p.block_table + static_cast<long long>(sg.b) * p.bt_stride;
+        const int npages = (L + kPage - 1) / kPage;
+        for (int jb = sg.t0; jb < sg.t1 && ok; jb += 32) {
+          const int cnt = min(32, sg.t1 - jb);
+          int my_page = -1;
+          const int pi = 2 * (jb + lane) + static_cast<int>(tok);
+          if (lane < cnt && pi < npages && pi < p.bt_stride) {
+            const int pg = bt_row[pi];
+            my_page = (pg >= 0 && pg < p.num_pages) ? pg : -1;
+          }
+          for (int jj = 0; jj < cnt && ok; ++jj) {
+            const int page = __shfl_sync(0xffffffffu, my_page, jj);
+            const int y = page >= 0 ? page * kPage : static_cast<int>(p.num_pages) * kPage;
+            for (int c = 0; c < kNumChunks; ++c) {
+              if (!(ok = claim(kPageChunk))) break;
+              if (lane == 0)
+                tma_load_2d_pair(kslot(u % kKSlots), &tm_kv, c * kChunk, y, rKF + 8u * ((u % kKSlots) / kKGroup));
+              ++u;
+            }
+          }
+        }
+        ++nseg;
+      }
+      // the last slot group may be partly used: empty uses complete its barrier
+      while (ok && u % kKGroup != 0) {
+        if (!(ok = claim(0))) break;
+        ++u;
+      }
+      issued = u;
+      if (!ok && lane == 0) {  // let copies in flight land before the CTA goes away
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < kDrainNs / 8) {
+        }
+      }
+    } else {
+      // Value ranks: per page, this rank's 256 value dims.
+      Ring<kVSlots> rv;
+      while (ok && it.next(sg)) {
+        const int L = max(p.cache_lens[sg.b], 0);
+        const int* bt_row = p.block_table + static_cast<long long>(sg.b) * p.bt_stride;
+        const int npages = (L + kPage - 1) / kPage;
+        for (int jb = sg.t0; jb < sg.t1 && ok; jb += 32) {
+          const int cnt = min(32, sg.t1 - jb);
+          int pg2[2] = {-1, -1};
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int pi = 2 * (jb + lane) + e;
+            if (lane < cnt && pi < npages && pi < p.bt_stride) {
+              const int pg = bt_row[pi];
+              pg2[e] = (pg >= 0 && pg < p.num_pages) ? pg : -1;
+            }
+          }
+          for (int jj = 0; jj < cnt && ok; ++jj) {
+#pragma unroll 1
+            for (int e = 0; e < 2; ++e, rv.advance()) {
+              const int page = __shfl_sync(0xffffffffu, e ? pg2[1] : pg2[0], jj);
+              if (!(ok = warp_wait(bar(kVE + rv.idx), rv.phase ^ 1u, ctl))) break;
+              if (lane == 0) {
+                const int y = page >= 0 ? page * kPage : static_cast<int>(p.num_pages) * kPage;
+                mbar_arrive_expect_tx(bar(kVF + rv.idx), kVPage);
+#pragma unroll
+                for (int lc = 0; lc < 4; ++lc) {
+                  const int gc = (lc >> 1) * 4 + 2 * static_cast<int>(tok) + (lc & 1);
+                  tma_load_2d(vslot(rv.idx) + lc * kPageChunk, &tm_kv, gc * kChunk, y, bar(kVF + rv.idx));
+                }
+              }
+              ++issued;
+            }
+          }
+        }
+      }
+      if (!ok && lane == 0) {
+        for (uint32_t k = 0; k < static_cast<uint32_t>(kVSlots) && k < issued; ++k) {
+          const uint32_t t = issued - 1 - k;
+          drain_bar(bar(kVF + t % kVSlots), (t / kVSlots) & 1u);
+        }
+      }
+    }
+  } else if (!score_rank && warp < kMmaWarp) {
+    // ================================================= V conversion (value ranks, warps 4-15)
+    const int ptid = threadIdx.x - 128;
+    const uint32_t rVR = mapa(bar(kVR), 2);
+    constexpr int kPieces = kVPage / 16;  // 2048 pieces of 16 B
+    SegIter it(p, unit);
+    Seg sg;
+    Ring<kVSlots> rv;
+    bool stop = false;  // the twelve warps vote at every named barrier
+    while (!stop && it.next(sg)) {
+      const int L = max(p.cache_lens[sg.b], 0);
+      for (int j = sg.t0; j < sg.t1 && !stop; ++j) {
+        for (int e = 0; e < 2; ++e, rv.advance()) {
+          const bool ok = warp_wait(bar(kVF + rv.idx), rv.phase, ctl);
+          if (!named_bar_all(6, kConvThreads, ok)) {
+            stop = true;
+            break;
+          }
+          const uint32_t stg = vslot(rv.idx);
+          const int r_end = L - j * kTileRows - e * kPage;  // rows >= r_end lie past the cache end: zero them
+          if (r_end >= kPage) {
+            if (!kBf16PV) {
+#pragma unroll 4
+              for (int piece = ptid; piece < kPieces; piece += kConvThreads) {
+                const uint32_t a = stg + 16u * piece;
+                const uint4 v = ld_shared_v4u(a);
+                st_shared_v4(a, bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z),
+                             bf16x2_to_f16x2(v.w));
+              }
+            }
+          } else {
+            for (int piece = ptid; piece < kPieces; piece += kConvThreads) {
+              const uint32_t a = stg + 16u * piece;
+              const int r = (piece & 511) >> 3;  // the swizzle only permutes pieces within a row
+              if (r >= r_end) {
+                st_shared_zero16(a);
+              } else if (!kBf16PV) {
+                const uint4 v = ld_shared_v4u(a);
+                st_shared_v4(a, bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z),
+                             bf16x2_to_f16x2(v.w));
+              }
+            }
+          }
+          fence_proxy_async_smem();
+          named_bar_sync(6, kConvThreads);
+          if (ptid == 0) mbar_arrive_remote(rVR + 8u * rv.idx);
+        }
+      }
+    }
+  }
+
+  // ======================================================= teardown
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // no CTA touches another's shared memory after this
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, kTmemCols);
+  }
+}
+
+template <bool kBf16PV>
+void cluster_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, int num_clusters, cudaStream_t stream) {
+  cfg = cudaLaunchConfig_t{};
+  cfg.gridDim = dim3(4 * num_clusters, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 4;  // two SM pairs
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+}
+
+}  // namespace mtp
+
+// ------------------------------------------------------------------ host side
+cudaError_t mtp_set_attrs() {
+  cudaError_t e = cudaFuncSetAttribute(mtp::mla_decode_mtp_kernel<false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, mtp::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(mtp::mla_decode_mtp_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              mtp::kSmemBytes);
+}
+
+// Co-resident 4-CTA clusters of the two-token kernel on the current device.
+cudaError_t mtp_max_clusters(int* n, int num_clusters_hint) {
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[1];
+  mtp::cluster_config<false>(cfg, attr, num_clusters_hint, nullptr);
+  return cudaOccupancyMaxActiveClusters(n, mtp::mla_decode_mtp_kernel<false>, &cfg);
+}
+
+cudaError_t mtp_launch(bool bf16_pv, int num_clusters, cudaStream_t stream, const DecodeParams& p,
+                       const CUtensorMap& tm_q, const CUtensorMap& tm_kv) {
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[1];
+  mtp::cluster_config<false>(cfg, attr, num_clusters, stream);
+  return bf16_pv ? cudaLaunchKernelEx(&cfg, mtp::mla_decode_mtp_kernel<true>, p, tm_q, tm_kv)
+                 : cudaLaunchKernelEx(&cfg, mtp::mla_decode_mtp_kernel<false>, p, tm_q, tm_kv);
+}
+
+}  // namespace mla

@@ -1,10 +1,11 @@
 // plan.cuh — split-KV partition of a decode step (shared by the device plan
 // kernel and the host mirror).
 //
-// Work unit: one 64-token tile of one request.  Request b has
-// n_b = ceil(len_b / 64) tiles (ceil(topk / 64) for top-k lists) and costs
-// n_b + C0 when n_b > 0, C0 standing for the per-split fixed work (loading
-// the 128x576 query block and writing the 128x512 output block).  Requests
+// Work unit: one tile of one request: 64 cached rows, or 128 on the
+// two-token dense path (whose tiles are two pages; see plan_tile_rows).
+// Request b has n_b = ceil(len_b / rows) tiles (ceil(topk / 64) for top-k
+// lists) and costs n_b + C0 when n_b > 0, C0 standing for the per-split fixed
+// work (loading the query block and writing the output block).  Requests
 // are laid end to end on a cost line; unit u owns the cost interval
 // [u*W, (u+1)*W), W = max(ceil(total / U), MIN_W).  A cut that falls inside
 // a request's fixed-cost prefix snaps to the request start; a cut inside its
@@ -20,7 +21,7 @@ constexpr int kPlanC0 = 2;       // fixed cost of a split, in tiles
 constexpr int kPlanMinTiles = 4; // a unit takes at least this many tiles
 
 struct ReqInfo {   // per request, int4 in the workspace
-  int n_tiles;     // 64-token tiles
+  int n_tiles;     // tiles (64 or 128 rows, see plan_tile_rows)
   int n_splits;    // units touching it (0 = nothing to attend to)
   int first_slot;  // partial-result slot of split 0 (only if n_splits > 1)
   int cost_prefix; // exclusive prefix of costs
@@ -30,9 +31,15 @@ struct UnitInfo {  // per unit, 5 ints in the workspace
   int begin_req, begin_tile, end_req, end_tile, first_split;
 };
 
-__host__ __device__ inline int plan_tiles(int len, int topk) {
+// Rows per tile: the two-token (s_q = 2) dense kernel walks two pages at a
+// time; every other path one page (or 64 top-k entries).
+__host__ __device__ inline int plan_tile_rows(int s_q, int topk) {
+  return (s_q == 2 && topk == 0) ? 128 : 64;
+}
+
+__host__ __device__ inline int plan_tiles(int len, int topk, int tile_rows) {
   if (topk > 0) return (topk + 63) / 64;
-  return len > 0 ? (len + 63) / 64 : 0;
+  return len > 0 ? (len + tile_rows - 1) / tile_rows : 0;
 }
 
 __host__ __device__ inline int plan_cost(int n_tiles) { return n_tiles > 0 ? n_tiles + kPlanC0 : 0; }

@@ -30,11 +30,12 @@ def _build():
     assert torch.cuda.is_available()
 
 
-def run(w, out_fp32=True, num_units=0, validate=False, q=None, kv=None, table=None, topk_idx="same"):
+def run(w, out_fp32=True, num_units=0, validate=False, q=None, kv=None, table=None, topk_idx="same",
+        bf16_pv=False):
     o, lse = m.decode_step(w.q if q is None else q, w.kv if kv is None else kv,
                            w.block_table if table is None else table, w.cache_lens, w.softmax_scale,
                            causal=w.causal, topk_idx=w.topk_idx if topk_idx == "same" else topk_idx,
-                           out_fp32=out_fp32, num_units=num_units, validate=validate)
+                           out_fp32=out_fp32, num_units=num_units, validate=validate, bf16_pv=bf16_pv)
     torch.cuda.synchronize()
     return o.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64)
 
@@ -167,6 +168,67 @@ def test_garbage_past_the_end_of_the_last_page_is_ignored():
     assert_close(o, lse, o_ref, lse_ref)
 
 
+# ---------------------------------------------------------------- two query tokens (paired-SM kernel)
+
+@pytest.mark.parametrize("causal", [True, False], ids=["causal", "full"])
+@pytest.mark.parametrize("L", [1, 2, 63, 64, 65, 127, 128, 129, 191, 255, 257])
+def test_two_token_lengths_around_tile_edges(L, causal):
+    # tiles are two pages: lengths that end in the first page of a tile, at a
+    # page edge, one past it, and in the second page
+    w = wl.make_workload(f"mtp{L}", [L, 2 * L + 3, 129], s_q=2, causal=causal, seed=L, device="cuda")
+    o_ref, lse_ref = reference(w)
+    o, lse = run(w)
+    assert_close(o, lse, o_ref, lse_ref)
+
+
+@pytest.mark.parametrize("bf16_pv", [False, True], ids=["f16pv", "bf16pv"])
+def test_two_token_value_precision_modes(bf16_pv):
+    w = wl.make_config("mtp_b64", device="cuda", batch=6, length=3000)
+    o_ref, lse_ref = reference(w)
+    o, lse = run(w, bf16_pv=bf16_pv)
+    assert_close(o, lse, o_ref, lse_ref)
+    ob, _ = run(w, out_fp32=False, bf16_pv=bf16_pv)
+    assert_close(ob, lse, o_ref, lse_ref)
+
+
+def test_two_token_full_size_bf16_pv_sampled():
+    w = wl.make_config("mtp_b64", device="cuda")
+    sel = [(b, t) for b in (3, 17, 40, 63) for t in range(2)]
+    o, lse = run(w, bf16_pv=True)
+    o_ref, lse_ref = reference(w, select=sel)
+    assert_close(o, lse, o_ref, lse_ref, select=sel)
+
+
+def test_two_token_split_across_units_matches_single_unit():
+    w = wl.make_workload("mtp_long", [8192, 300], s_q=2, causal=True, seed=21, device="cuda")
+    o_ref, lse_ref = reference(w)
+    o_many, lse_many = run(w)
+    o_one, lse_one = run(w, num_units=1)
+    assert_close(o_many, lse_many, o_ref, lse_ref)
+    assert_close(o_one, lse_one, o_ref, lse_ref)
+
+
+def test_two_token_garbage_past_the_end_is_ignored():
+    # request 0 has 70 rows: its tile spans pages 0-1, rows 70..127 are past the end
+    w = wl.make_workload("g2", [70, 10], s_q=2, causal=True, shuffle=False, seed=8, device="cuda")
+    o_ref, lse_ref = reference(w)
+    kv = w.kv.clone()
+    flat = kv.view(-1, 576)
+    nan = torch.tensor(float("nan"), dtype=torch.bfloat16, device="cuda")
+    flat[70:128] = nan
+    flat[128 + 10:192] = nan
+    o, lse = run(w, kv=kv)
+    assert np.isfinite(o).all()
+    assert_close(o, lse, o_ref, lse_ref)
+
+
+def test_two_token_sparse_uses_per_token_lists():
+    w = wl.make_workload("s2", [3000, 1500], s_q=2, topk=256, seed=23, device="cuda")
+    o_ref, lse_ref = reference(w)
+    o, lse = run(w)
+    assert_close(o, lse, o_ref, lse_ref)
+
+
 # ---------------------------------------------------------------- invariants
 
 def test_page_permutation_gives_identical_output():
@@ -186,6 +248,17 @@ def test_repeated_calls_are_bit_identical():
     a = run(w)
     b = run(w)
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_two_token_page_permutation_gives_identical_output():
+    w = wl.make_config("mtp_b64", device="cuda", batch=3, length=900)
+    o1, l1 = run(w)
+    perm = torch.randperm(w.num_pages, generator=torch.Generator().manual_seed(2)).cuda()
+    inv = torch.argsort(perm)
+    t = w.block_table.long()
+    table2 = torch.where(t >= 0, inv[t.clamp(min=0)], t).int()
+    o2, l2 = run(w, kv=w.kv[perm], table=table2)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
 
 
 def test_sparse_full_index_list_matches_dense():

@@ -33,10 +33,11 @@ def expand(um, rm):
     return units
 
 
-def check_plan(lens, U, topk=0):
-    um, rm = m.mla_decode_plan_host(lens, topk, U)
+def check_plan(lens, U, topk=0, s_q=1):
+    um, rm = m.mla_decode_plan_host(lens, s_q, topk, U)
     lens = np.asarray(lens)
-    ntiles = np.array([(k + 63) // 64 for k in ([topk] * len(lens) if topk else np.maximum(lens, 0))])
+    rows = 128 if (s_q == 2 and topk == 0) else 64  # the two-token dense kernel takes two pages per tile
+    ntiles = np.array([(k + rows - 1) // rows for k in ([topk] * len(lens) if topk else np.maximum(lens, 0))])
     assert np.array_equal(rm[:, 0], ntiles)
     units = expand(um, rm)
     flat = [w for u in units for w in u]
@@ -81,9 +82,20 @@ def test_random_lengths(seed):
     check_plan(lens, U)
 
 
+@pytest.mark.parametrize("seed", range(6))
+def test_random_lengths_two_tokens(seed):
+    rng = np.random.default_rng(100 + seed)
+    B = int(rng.integers(1, 200))
+    lens = rng.integers(0, 9000, B)
+    lens[rng.random(B) < 0.1] = 0
+    U = int(rng.integers(1, 60))
+    check_plan(lens, U, s_q=2)
+    check_plan(lens, U, topk=int(rng.integers(1, 3000)), s_q=2)
+
+
 def test_decode_workload_shapes():
     check_plan([4096] * 32, 74)
-    check_plan(np.random.default_rng(0).integers(1, 8193, 64), 37)
+    check_plan(np.random.default_rng(0).integers(1, 8193, 64), 36, s_q=2)
     check_plan([32768] * 128, 74)
     check_plan([65536] * 80, 74, topk=2048)
     check_plan([256], 74)
@@ -98,6 +110,11 @@ def test_one_long_request_is_split_across_all_units():
 def test_single_unit_never_splits():
     um, rm, units = check_plan([100, 5000, 1, 64], 1)
     assert (rm[:, 1] == 1).all()
+
+
+def test_two_token_tiles_are_two_pages():
+    um, rm, units = check_plan([1, 64, 65, 128, 129, 8192], 4, s_q=2)
+    assert list(rm[:, 0]) == [1, 1, 1, 1, 2, 64]
 
 
 def test_empty_requests_have_no_work():
