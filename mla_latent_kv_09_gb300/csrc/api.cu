@@ -30,7 +30,7 @@ cudaError_t decode_launch(bool sparse, int num_clusters, cudaStream_t stream, co
 cudaError_t mtp_set_attrs();
 cudaError_t mtp_max_clusters(int* n, int num_clusters_hint);
 cudaError_t mtp_launch(bool bf16_pv, int num_clusters, cudaStream_t stream, const DecodeParams& p,
-                       const CUtensorMap& tm_q, const CUtensorMap& tm_kv);
+                       const CUtensorMap& tm_q, const CUtensorMap& tm_k3, const CUtensorMap& tm_v2);
 }  // namespace mla
 
 using namespace mla;
@@ -136,6 +136,22 @@ int encode_2d(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows
   const cuuint32_t box[2] = {static_cast<cuuint32_t>(kChunk), box_rows};
   const cuuint32_t estr[2] = {1, 1};
   const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+                        estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MLA_OK : MLA_ERR_CUDA;
+}
+
+// The cache as a 3-D tensor (x: column within a 64-column chunk, y: row,
+// z: chunk): one box fetches `box_chunks` chunks of 64 rows in one request.
+int encode_kv_3d(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_chunks) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return MLA_ERR_CUDA;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kChunk), static_cast<cuuint64_t>(rows),
+                              static_cast<cuuint64_t>(kNumChunks)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kDqk) * 2, static_cast<cuuint64_t>(kChunk) * 2};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(kChunk), static_cast<cuuint32_t>(kPage), box_chunks};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
                         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? MLA_OK : MLA_ERR_CUDA;
@@ -290,9 +306,16 @@ int mla_decode(const void* q, const void* kv_cache, int64_t num_pages, const int
 
   // two query tokens, dense: both tokens share every tile (4-CTA clusters,
   // paired-SM MMAs); otherwise one 2-CTA cluster per (unit, token)
-  const cudaError_t e = pair_path
-                            ? mtp_launch((flags & MLA_FLAG_BF16_PV) != 0, U, s, p, tm_q, tm_kv)
-                            : decode_launch(topk_idx != nullptr, U * s_q, s, p, tm_q, tm_kv);
+  cudaError_t e;
+  if (pair_path) {
+    CUtensorMap tm_k3, tm_v2;  // K: three chunks (a slot group) per load; V: two chunks per load
+    const uint64_t rows = static_cast<uint64_t>(num_pages) * kPage;
+    if ((rc = encode_kv_3d(&tm_k3, kv_cache, rows, 3)) != MLA_OK) return rc;
+    if ((rc = encode_kv_3d(&tm_v2, kv_cache, rows, 2)) != MLA_OK) return rc;
+    e = mtp_launch((flags & MLA_FLAG_BF16_PV) != 0, U, s, p, tm_q, tm_k3, tm_v2);
+  } else {
+    e = decode_launch(topk_idx != nullptr, U * s_q, s, p, tm_q, tm_kv);
+  }
   if (e != cudaSuccess) {
     cudaGetLastError();
     return MLA_ERR_CUDA;

@@ -36,11 +36,21 @@
 // P and V are fp16 (11 significant bits on the softmax weights; values must
 // stay below 65504 in magnitude), or bf16 in the kBf16PV variant.
 //
-// Warps (608 threads).  Score ranks: 0-15 softmax (warp w: head rows
-// 32 (w % 4) .., key columns 32 (w / 4) .. of each tile), 16 MMA issue on rank
-// 0 and tensor-memory owner, 17 TMA producer, 18 P shipper.  Value ranks: 0-3
-// O rescale and epilogue (thread i = head row i), 4-15 V conversion, 16 MMA
-// issue on rank 2 and tensor-memory owner, 17 TMA producer.
+// Warps (640 threads).  Score ranks: 0-15 softmax (warp w: head rows
+// 32 (w % 4) .., key columns 32 (w / 4) .. of each tile), 16 and 19 MMA issue
+// on rank 0 (even and odd tiles; 16 also owns tensor memory and moves Q in),
+// 17 TMA producer, 18 P shipper.  Value ranks: 0-3 O rescale and epilogue
+// (thread i = head row i), 4-15 V conversion, 16 MMA issue on rank 2 and
+// tensor-memory owner, 17 TMA producer.
+//
+// Two threads issue the score MMAs, alternating tiles: a single issuing
+// thread leaves the tensor pipe idle while it waits on a barrier (a wait is
+// ~150 cycles even when the barrier is complete, and the MMA queue holds
+// little more than one MMA).  Each issuer does all the waits of its tile
+// (score buffer free, three slot groups landed) while the other issues, then
+// takes an issue token from the other and issues its 36 MMAs without a wait,
+// passing the token on after 24 of them.  Tiles thus follow each other in
+// the pipe, which keeps the chunk ring's full lookahead.
 //
 // P travels as one bulk copy per tile: the softmax warps write it into a
 // local copy laid out as the value rank's A operand; the shipper warp sends
@@ -100,24 +110,26 @@ constexpr uint32_t kColS = 0;    // score ranks: two 128-column score buffers
 constexpr uint32_t kColQ = 256;  // score ranks: Q dims 0..511, 8 chunks of 32 columns
 constexpr uint32_t kColO = 0;    // value ranks: O, 512 columns
 
-constexpr int kThreads = 608;                    // 19 warps
+constexpr int kThreads = 640;                    // 20 warps
 constexpr int kSoftmaxWarps = 16;
 constexpr int kConvThreads = 384;                // value ranks: warps 4-15
 constexpr int kMmaWarp = 16;
 constexpr int kTmaWarp = 17;
 constexpr int kShipWarp = 18;                    // score ranks: P shipper
+constexpr int kMma2Warp = 19;                    // rank 0: issues the score MMAs of odd tiles
 constexpr float kRescaleLog2 = 8.0f;
+constexpr int kL2Ahead = 3;  // score ranks: tiles whose page is prefetched into L2 ahead of the ring
 
 constexpr uint16_t kScoreMask = 0x3;  // ranks 0, 1
 constexpr uint16_t kValueMask = 0xC;  // ranks 2, 3
 
 enum Bar {
-  kKF = 0,        // [6] rank 0: slot group landed in both score ranks (3 arrivals + TMA tx of both)
+  kKF = 0,        // [6] rank 0: slot group landed in both score ranks (1 arrival + TMA tx of both)
   kKE = 6,        // [6] score ranks: slot group free (commit from rank 0)
   kQRF = 12,      // [2] rank 0: Q RoPE buffer landed in both score ranks (TMA tx of both)
-  kQFree = 14,    // [2] score ranks: the score MMAs of the segment using that RoPE buffer finished
-  kQF = 36,       // score ranks: a segment's last score MMA finished (Q may be replaced)
-  kQR = 37,       // (unused)
+  kQFree = 14,    // [2] score ranks: both issuers' score MMAs of the segment using that RoPE buffer finished
+  kQF = 36,       // rank 0: both issuers' score MMAs of a segment finished (Q may be replaced)
+  kQC = 37,       // rank 0: Q of the segment copied into tensor memory (commit from the first issuer)
   kSF = 38,       // [2] score ranks: scores ready (commit from rank 0)
   kSE = 40,       // [2] rank 0: scores read (one arrival per row quarter of both ranks)
   kPFree = 42,    // [2] score ranks: PV finished with that P slot (commit from rank 2)
@@ -132,7 +144,10 @@ enum Bar {
   kMmaDone = 64,  // teardown
   kPsFull = 65,   // score ranks: the local P copy is written (one arrival per softmax warp)
   kPsFree = 66,   // score ranks: the bulk copy has read the local P copy
-  kNumBars = 67
+  kMmaDone2 = 67, // teardown (second issuer)
+  kHand = 68,     // [2] rank 0: score-MMA issue token (tile parity): the issuer of tile g may start
+                  //     once the issuer of tile g - 1 has issued two thirds of its MMAs
+  kNumBars = 70
 };
 static_assert(kNumBars * 8 + 16 <= kBarBytes, "barrier block");
 
@@ -167,7 +182,7 @@ __host__ __device__ constexpr uint32_t p_message_bytes(bool last) {
 template <bool kBf16PV>
 __global__ void __launch_bounds__(kThreads, 1)
 mla_decode_mtp_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tm_q,
-                      const __grid_constant__ CUtensorMap tm_kv) {
+                      const __grid_constant__ CUtensorMap tm_k3, const __grid_constant__ CUtensorMap tm_v2) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t mis = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* smem = smem_raw + mis;
@@ -196,13 +211,17 @@ mla_decode_mtp_kernel(const __grid_constant__ DecodeParams p, const __grid_const
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kKGroups; ++i) {
-      mbar_init(bar(kKF + i), kKGroup);
+      mbar_init(bar(kKF + i), 1);
       mbar_init(bar(kKE + i), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(kQRF + i), 1);
-      mbar_init(bar(kQFree + i), 1);
+      mbar_init(bar(kQFree + i), 2);
     }
+    mbar_init(bar(kQC), 1);
+    mbar_init(bar(kMmaDone2), 1);
+    mbar_init(bar(kHand), 1);
+    mbar_init(bar(kHand + 1), 1);
     for (int i = 0; i < kVSlots; ++i) {
       mbar_init(bar(kVF + i), 1);
       mbar_init(bar(kVE + i), 1);
@@ -216,7 +235,7 @@ mla_decode_mtp_kernel(const __grid_constant__ DecodeParams p, const __grid_const
       mbar_init(bar(kPR + i), 2);
       mbar_init(bar(kPD + i), 1);
     }
-    mbar_init(bar(kQF), 1);
+    mbar_init(bar(kQF), 2);
     mbar_init(bar(kOF), 1);
     mbar_init(bar(kOE), 2);
     mbar_init(bar(kMmaDone), 1);
@@ -231,7 +250,7 @@ mla_decode_mtp_kernel(const __grid_constant__ DecodeParams p, const __grid_const
   }
   if (warp == kTmaWarp && lane == 0) {
     tma_prefetch_desc(&tm_q);
-    tma_prefetch_desc(&tm_kv);
+    tma_prefetch_desc(score_rank ? &tm_k3 : &tm_v2);
   }
   tc_fence_before();
   __syncthreads();
@@ -247,6 +266,95 @@ mla_decode_mtp_kernel(const __grid_constant__ DecodeParams p, const __grid_const
   ctl.status = p.ws_hdr + kHdrStatus;
   const float NEG_INF = -__int_as_float(0x7f800000);
   const int U = p.num_units;
+
+  // ======================================================= score-MMA issue (rank 0)
+  // The chunk ring is consumed in "uses" of one 8 KiB slot: a K chunk, half
+  // of a Q chunk (a Q chunk is two adjacent slots) or a pad.  Per segment:
+  // 2 or 5 pads (so that Q starts on a slot = 2 mod 6: even, and its 16 uses
+  // end on a group boundary), 16 Q uses, then 9 uses per tile; every tile is
+  // three whole slot groups, owned by the issuer of that tile.  Issuer A
+  // (even tiles, score buffer 0) also copies Q into tensor memory; issuer B
+  // (odd tiles, score buffer 1) waits until that copy has completed.
+  auto issue_scores = [&](bool is_a) {
+    SegIter it(p, unit);
+    Seg sg;
+    uint32_t g = 0, nseg = 0, u = 0;
+    bool ok = true;
+    const uint32_t kf0 = bar(kKF), ke0 = bar(kKE), slot0 = sbase + kOffStage;
+    const uint32_t own = is_a ? 0u : 1u;
+    while (ok && it.next(sg)) {
+      const uint32_t u_q = u + ((u % 6u == 0u) ? 2u : 5u);
+      const uint32_t u_t = u_q + 16u;  // first use of the segment's tiles (a group boundary)
+      if (is_a) {
+        if (nseg > 0 && !(ok = wait_bar<false>(bar(kQF), (nseg - 1u) & 1u, ctl))) break;
+        // pads and Q may span seven slot groups, one more than the ring: wait,
+        // copy and free chunk by chunk
+        uint32_t gw = u / kKGroup, gf = u / kKGroup;  // next group to wait for / to free
+        for (int i = 0; i < 8 && ok; ++i) {
+          const uint32_t ue = u_q + 2u * i + 2u;  // uses [.., ue) are consumed by this copy
+          for (; gw * kKGroup < ue && ok; ++gw) {
+            ok = wait_bar<true>(kf0 + 8u * (gw % kKGroups), (gw / kKGroups) & 1u, ctl);
+            tc_fence_after();
+          }
+          if (!ok) break;
+          const uint64_t qd = smem_desc(slot0 + ((u_q + 2u * i) % kKSlots) * kPageChunk, 16u, 1024u);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            tmem_cp_pair_128x256b(tmem + kColQ + 32u * i + 8u * kk, qd + static_cast<uint64_t>((32 * kk) >> 4));
+          for (; (gf + 1) * kKGroup <= ue; ++gf) umma_commit_pair(ke0 + 8u * (gf % kKGroups), kScoreMask);
+        }
+        if (!ok) break;
+        umma_commit_pair(bar(kQC), 1u << 0);
+      } else {
+        if (!(ok = wait_bar<false>(bar(kQC), nseg & 1u, ctl))) break;
+        tc_fence_after();
+      }
+      u = u_t;
+      if (!(ok = wait_bar<true>(bar(kQRF + (nseg & 1u)), (nseg >> 1) & 1u, ctl))) break;
+      const uint64_t qr0 = smem_desc(sbase + kOffQr + (nseg & 1u) * kQChunk, 16u, 1024u);
+      for (int j = sg.t0; j < sg.t1 && ok; ++j, ++g, u += kNumChunks) {
+        const uint32_t sb = g & 1u, ph = (g >> 1) & 1u;
+        if (sb != own) continue;
+        if (!(ok = wait_bar<true>(bar(kSE + sb), ph ^ 1u, ctl))) break;
+        for (uint32_t G = u / kKGroup; G < (u + kNumChunks) / kKGroup && ok; ++G)
+          ok = wait_bar<true>(kf0 + 8u * (G % kKGroups), (G / kKGroups) & 1u, ctl);
+        if (!ok) break;
+        if (g > 0 && !(ok = wait_bar<false>(bar(kHand + ((g - 1u) & 1u)), ((g - 1u) >> 1) & 1u, ctl))) break;
+        tc_fence_after();
+        const uint32_t dS = tmem + kColS + 128u * sb;
+        // K = 576 in 36 steps of 16, one 64-dim chunk per slot
+#pragma unroll
+        for (int c = 0; c < kNumChunks; ++c) {
+          const uint32_t uc = u + c;
+          const uint32_t G = uc / kKGroup;
+          if (c == 6) mbar_arrive_relaxed(bar(kHand + sb));  // the other issuer may start its tile
+          const uint64_t bd = smem_desc(slot0 + (uc % kKSlots) * kPageChunk, 16u, 1024u);
+          if (c < 8) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              umma_pair_ta(dS, tmem + kColQ + 32u * c + 8u * kk, bd + static_cast<uint64_t>((32 * kk) >> 4),
+                           kIdescQK, (c | kk) != 0 ? 1u : 0u);
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              umma_pair_sa(dS, qr0 + static_cast<uint64_t>((32 * kk) >> 4),
+                           bd + static_cast<uint64_t>((32 * kk) >> 4), kIdescQK, 1u);
+          }
+          if (c % kKGroup == kKGroup - 1) umma_commit_pair(ke0 + 8u * (G % kKGroups), kScoreMask);
+        }
+        if (!ok) break;
+        umma_commit_pair(bar(kSF + sb), kScoreMask);
+      }
+      if (!ok) break;
+      // this issuer's score MMAs of the segment: Q and the RoPE buffer may be replaced after both
+      umma_commit_pair(bar(kQF), 1u << 0);
+      umma_commit_pair(bar(kQFree + (nseg & 1u)), kScoreMask);
+      ++nseg;
+    }
+    const uint32_t done = bar(is_a ? kMmaDone : kMmaDone2);
+    umma_commit_pair(done, 1u << 0);  // every MMA this thread issued has finished
+    drain_bar(done, 0);
+  };
 
   if (score_rank && warp < kSoftmaxWarps) {
     // ================================================= softmax (score ranks)
@@ -313,7 +421,8 @@ mla_decode_mtp_kernel(const __grid_constant__ DecodeParams p, const __grid_const
           stop = true;
           break;
         }
-        if (lead && lane == 0) mbar_arrive_remote(rSE + 8u * sb);  // the quarter has read its scores
+        // the quarter has read its scores (tcgen05.wait::ld completed the reads)
+        if (lead && lane == 0) mbar_arrive_remote_relaxed(rSE + 8u * sb);
         const float* xm = xmax + sb * 4 * kHeads + row;
         const float mt = fmaxf(fmaxf(xm[0], xm[kHeads]), fmaxf(xm[2 * kHeads], xm[3 * kHeads])) * p.scale_log2;
 
@@ -395,7 +504,7 @@ mla_decode_mtp_kernel(const __grid_constant__ DecodeParams p, const __grid_const
           if (j == sg.t1 - 1) bulk_copy_s2c(rFin + sb * kHeads * 4u, sbase + kOffFinS, kHeads * 4u, mbar);
           bulk_commit();
           bulk_wait_read();
-          mbar_arrive(bar(kPsFree));
+          mbar_arrive_relaxed(bar(kPsFree));  // execution token: the copy has read the local P
         }
       }
       bulk_wait_all();  // copies out of this CTA's memory are complete
@@ -494,93 +603,16 @@ mla_decode_mtp_kernel(const __grid_constant__ DecodeParams p, const __grid_const
           }
           tc_fence_before();
           named_bar_sync(5, 128);
-          if (row == 0) mbar_arrive_remote(rOE);
+          if (row == 0) mbar_arrive_remote_relaxed(rOE);  // O read (tcgen05.wait::ld completed)
         }
       }
       ++nseg;
     }
-  } else if (warp == kMmaWarp) {
-    // ================================================= MMA issue (ranks 0 and 2, one thread)
+  } else if (warp == kMmaWarp || warp == kMma2Warp) {
+    // ================================================= MMA issue (rank 0: two threads, rank 2: one)
     if (lane == 0 && rank == 0) {
-      // The ring is consumed in "uses" of one 8 KiB slot: a K chunk (1 use),
-      // half of a Q chunk (1 use; a Q chunk is two adjacent slots) or a pad
-      // (1 use, keeps Q chunks on even slots).  Slot groups are waited for
-      // before their first use and freed after their last.  Plain counters
-      // (no captures): this loop must issue an MMA every ~64 cycles.
-      SegIter it(p, unit);
-      Seg sg;
-      uint32_t g = 0, nseg = 0;
-      uint32_t u = 0;       // uses consumed
-      uint32_t waited = 0;  // slot-group phases waited for
-      bool ok = true;
-      const uint32_t kf0 = bar(kKF), ke0 = bar(kKE), slot0 = sbase + kOffStage;
-      while (ok && it.next(sg)) {
-        // Q: the old one is free once the previous segment's score MMAs finish
-        if (nseg > 0 && !(ok = wait_bar<false>(bar(kQF), (nseg - 1u) & 1u, ctl))) break;
-        tc_fence_after();
-        const uint32_t u_q = u + (u & 1u);  // first Q use (after a pad)
-        for (int i = 0; i < 8 && ok; ++i) {
-          const uint32_t ue = u_q + 2u * i + 2u;  // uses [.., ue) must have landed
-          while (waited * kKGroup < ue) {
-            if (!(ok = wait_bar<true>(kf0 + 8u * (waited % kKGroups), (waited / kKGroups) & 1u, ctl))) break;
-            tc_fence_after();
-            ++waited;
-          }
-          if (!ok) break;
-          const uint32_t uq = u_q + 2u * i;
-          const uint64_t qd = smem_desc(slot0 + (uq % kKSlots) * kPageChunk, 16u, 1024u);  // two adjacent slots
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            tmem_cp_pair_128x256b(tmem + kColQ + 32u * i + 8u * kk, qd + static_cast<uint64_t>((32 * kk) >> 4));
-          // free the groups all of whose uses are now consumed
-          for (uint32_t f = u / kKGroup; (f + 1) * kKGroup <= ue; ++f)
-            umma_commit_pair(ke0 + 8u * (f % kKGroups), kScoreMask);
-          u = ue;
-        }
-        if (!ok) break;
-        if (!(ok = wait_bar<true>(bar(kQRF + (nseg & 1u)), (nseg >> 1) & 1u, ctl))) break;
-        const uint64_t qr0 = smem_desc(sbase + kOffQr + (nseg & 1u) * kQChunk, 16u, 1024u);
-        for (int j = sg.t0; j < sg.t1 && ok; ++j, ++g) {
-          const uint32_t sb = g & 1u, ph = (g >> 1) & 1u;
-          if (!(ok = wait_bar<true>(bar(kSE + sb), ph ^ 1u, ctl))) break;
-          tc_fence_after();
-          const uint32_t dS = tmem + kColS + 128u * sb;
-          // K = 576 in 36 steps of 16, one 64-dim chunk per slot
-#pragma unroll
-          for (int c = 0; c < kNumChunks; ++c) {
-            const uint32_t uc = u + c;
-            if (waited * kKGroup <= uc) {  // uc opens a new slot group
-              if (!(ok = wait_bar<true>(kf0 + 8u * (waited % kKGroups), (waited / kKGroups) & 1u, ctl))) break;
-              tc_fence_after();
-              ++waited;
-            }
-            const uint64_t bd = smem_desc(slot0 + (uc % kKSlots) * kPageChunk, 16u, 1024u);
-            if (c < 8) {
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                umma_pair_ta(dS, tmem + kColQ + 32u * c + 8u * kk, bd + static_cast<uint64_t>((32 * kk) >> 4),
-                             kIdescQK, (c | kk) != 0 ? 1u : 0u);
-            } else {
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                umma_pair_sa(dS, qr0 + static_cast<uint64_t>((32 * kk) >> 4),
-                             bd + static_cast<uint64_t>((32 * kk) >> 4), kIdescQK, 1u);
-            }
-            if ((uc + 1) % kKGroup == 0) umma_commit_pair(ke0 + 8u * ((uc / kKGroup) % kKGroups), kScoreMask);
-          }
-          if (!ok) break;
-          u += kNumChunks;
-          umma_commit_pair(bar(kSF + sb), kScoreMask);
-          if (j == sg.t1 - 1) {
-            umma_commit_pair(bar(kQF), kScoreMask);
-            umma_commit_pair(bar(kQFree + (nseg & 1u)), kScoreMask);
-          }
-        }
-        ++nseg;
-      }
-      umma_commit_pair(bar(kMmaDone), 1u << 0);  // every MMA issued so far has finished
-      drain_bar(bar(kMmaDone), 0);
-    } else if (lane == 0 && rank == 2) {
+      issue_scores(warp == kMmaWarp);
+    } else if (lane == 0 && rank == 2 && warp == kMmaWarp) {
       SegIter it(p, unit);
       Seg sg;
       Ring<kVSlots> rv;
@@ -633,16 +665,23 @@ mla_decode_mtp_kernel(const __grid_constant__ DecodeParams p, const __grid_const
     if (score_rank) {
       // Both score ranks fill their own chunk slots; every copy completes on
       // rank 0's barriers, which rank 0 arms with the bytes of both.  The use
-      // sequence is the MMA thread's: per segment a pad if needed, 16 Q
-      // halves, then 9 K chunks per tile.
+      // sequence is the issuers': per segment 2 or 5 pads, 16 Q halves, then
+      // 9 K chunks per tile.
       const uint32_t rKF = mapa(bar(kKF), 0);
       const uint32_t rQRF = mapa(bar(kQRF), 0);
       uint32_t u = 0, nseg = 0;
-      // claim the next slot: wait for its group to be free at the group's first use
+      // claim the next slot: wait for its group to be free at the group's
+      // first use, add its bytes (both ranks) to the group's landing barrier,
+      // and arrive once at the group's last use.  Relaxed forms: the
+      // producer writes none of the data, and release semantics make each
+      // barrier operation wait for the thread's earlier memory operations.
       auto claim = [&](uint32_t bytes) -> bool {
         const uint32_t sl = u % kKSlots, grp = sl / kKGroup;
         if (sl % kKGroup == 0 && !warp_wait(bar(kKE + grp), ((u / kKSlots) & 1u) ^ 1u, ctl)) return false;
-        if (lane == 0 && tok == 0) mbar_arrive_expect_tx(bar(kKF + grp), 2u * bytes);
+        if (lane == 0 && tok == 0) {
+          if (sl % kKGroup == kKGroup - 1) mbar_arrive_expect_tx_relaxed(bar(kKF + grp), 2u * bytes);
+          else if (bytes) mbar_expect_tx_relaxed(bar(kKF + grp), 2u * bytes);
+        }
         return true;
       };
       while (ok && it.next(sg)) {
@@ -651,12 +690,12 @@ mla_decode_mtp_kernel(const __grid_constant__ DecodeParams p, const __grid_const
         // RoPE part of Q into buffer nseg % 2 once segment nseg - 2 is done with it
         if (nseg >= 2 && !(ok = warp_wait(bar(kQFree + (nseg & 1u)), ((nseg - 2u) >> 1) & 1u, ctl))) break;
         if (lane == 0) {
-          if (tok == 0) mbar_arrive_expect_tx(bar(kQRF + (nseg & 1u)), 2u * kQChunk);
+          if (tok == 0) mbar_arrive_expect_tx_relaxed(bar(kQRF + (nseg & 1u)), 2u * kQChunk);
           for (int h = 0; h < 2; ++h)
             tma_load_2d_pair(sbase + kOffQr + (nseg & 1u) * kQChunk + h * kPageChunk, &tm_q, 8 * kChunk,
                              qy + h * kPage, rQRF + 8u * (nseg & 1u));
         }
-        if (u & 1u) {  // pad
+        for (uint32_t npad = (u % 6u == 0u) ? 2u : 5u; npad > 0 && ok; --npad) {  // pads
           if (!(ok = claim(0))) break;
           ++u;
         }
@@ -680,23 +719,29 @@ mla_decode_mtp_kernel(const __grid_constant__ DecodeParams p, const __grid_const
             const int pg = bt_row[pi];
             my_page = (pg >= 0 && pg < p.num_pages) ? pg : -1;
           }
+          // the ring holds two tiles, less than the load latency under load:
+          // pages a few tiles ahead are pulled into L2 (no shared memory needed)
+          if (lane < kL2Ahead && lane < cnt && my_page >= 0)
+            bulk_prefetch_l2(p.kv + static_cast<long long>(my_page) * kPage * kDqk, kPage * kDqk * 2);
           for (int jj = 0; jj < cnt && ok; ++jj) {
             const int page = __shfl_sync(0xffffffffu, my_page, jj);
+            const int pf = __shfl_sync(0xffffffffu, my_page, min(jj + kL2Ahead, 31));
+            if (lane == 0 && jj + kL2Ahead < cnt && pf >= 0)
+              bulk_prefetch_l2(p.kv + static_cast<long long>(pf) * kPage * kDqk, kPage * kDqk * 2);
             const int y = page >= 0 ? page * kPage : static_cast<int>(p.num_pages) * kPage;
-            for (int c = 0; c < kNumChunks; ++c) {
-              if (!(ok = claim(kPageChunk))) break;
-              if (lane == 0)
-                tma_load_2d_pair(kslot(u % kKSlots), &tm_kv, c * kChunk, y, rKF + 8u * ((u % kKSlots) / kKGroup));
-              ++u;
+            // a tile is three whole slot groups: one 3-chunk load per group
+            for (int c = 0; c < kNumChunks; c += kKGroup) {
+              const uint32_t sl = u % kKSlots, grp = sl / kKGroup;
+              if (!(ok = warp_wait(bar(kKE + grp), ((u / kKSlots) & 1u) ^ 1u, ctl))) break;
+              if (lane == 0) {
+                if (tok == 0) mbar_arrive_expect_tx_relaxed(bar(kKF + grp), 2u * kKGroup * kPageChunk);
+                tma_load_3d_pair(kslot(sl), &tm_k3, 0, y, c, rKF + 8u * grp);
+              }
+              u += kKGroup;
             }
           }
         }
         ++nseg;
-      }
-      // the last slot group may be partly used: empty uses complete its barrier
-      while (ok && u % kKGroup != 0) {
-        if (!(ok = claim(0))) break;
-        ++u;
       }
       issued = u;
       if (!ok && lane == 0) {  // let copies in flight land before the CTA goes away
@@ -729,12 +774,12 @@ mla_decode_mtp_kernel(const __grid_constant__ DecodeParams p, const __grid_const
               if (!(ok = warp_wait(bar(kVE + rv.idx), rv.phase ^ 1u, ctl))) break;
               if (lane == 0) {
                 const int y = page >= 0 ? page * kPage : static_cast<int>(p.num_pages) * kPage;
-                mbar_arrive_expect_tx(bar(kVF + rv.idx), kVPage);
+                mbar_arrive_expect_tx_relaxed(bar(kVF + rv.idx), kVPage);
+                // chunks 2 tok, 2 tok + 1 and 4 + 2 tok, 5 + 2 tok: two loads of two chunks
 #pragma unroll
-                for (int lc = 0; lc < 4; ++lc) {
-                  const int gc = (lc >> 1) * 4 + 2 * static_cast<int>(tok) + (lc & 1);
-                  tma_load_2d(vslot(rv.idx) + lc * kPageChunk, &tm_kv, gc * kChunk, y, bar(kVF + rv.idx));
-                }
+                for (int h = 0; h < 2; ++h)
+                  tma_load_3d(vslot(rv.idx) + 2 * h * kPageChunk, &tm_v2, 0, y, 4 * h + 2 * static_cast<int>(tok),
+                              bar(kVF + rv.idx));
               }
               ++issued;
             }
@@ -844,12 +889,12 @@ cudaError_t mtp_max_clusters(int* n, int num_clusters_hint) {
 }
 
 cudaError_t mtp_launch(bool bf16_pv, int num_clusters, cudaStream_t stream, const DecodeParams& p,
-                       const CUtensorMap& tm_q, const CUtensorMap& tm_kv) {
+                       const CUtensorMap& tm_q, const CUtensorMap& tm_k3, const CUtensorMap& tm_v2) {
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[1];
   mtp::cluster_config<false>(cfg, attr, num_clusters, stream);
-  return bf16_pv ? cudaLaunchKernelEx(&cfg, mtp::mla_decode_mtp_kernel<true>, p, tm_q, tm_kv)
-                 : cudaLaunchKernelEx(&cfg, mtp::mla_decode_mtp_kernel<false>, p, tm_q, tm_kv);
+  return bf16_pv ? cudaLaunchKernelEx(&cfg, mtp::mla_decode_mtp_kernel<true>, p, tm_q, tm_k3, tm_v2)
+                 : cudaLaunchKernelEx(&cfg, mtp::mla_decode_mtp_kernel<false>, p, tm_q, tm_k3, tm_v2);
 }
 
 }  // namespace mla
