@@ -230,7 +230,7 @@ def run_ours(args, world, rank, local):
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     topk = w.topk
-    flags = (m.MLA_FLAG_CAUSAL if w.causal else 0) | (m.MLA_FLAG_BF16_PV if args.bf16_pv else 0)
+    flags = (m.MLA_FLAG_CAUSAL if w.causal else 0) | (m.MLA_FLAG_F16_PV if args.f16_pv else 0)
     U = ws.num_units
 
     def plan():
@@ -296,7 +296,7 @@ def run_ours(args, world, rank, local):
         def e2e_step():
             m.decode_step_host(pin["q"], pin["kv_cache"], pin["block_table"], pin["cache_lens"],
                                w.softmax_scale, device=dev, causal=w.causal, topk_idx=pin.get("topk_idx"),
-                               bf16_pv=args.bf16_pv, workspace=ws, dev_buffers=dbuf, out_host=o_h,
+                               f16_pv=args.f16_pv, workspace=ws, dev_buffers=dbuf, out_host=o_h,
                                lse_host=l_h)
 
         for _ in range(3):
@@ -364,8 +364,8 @@ def main():
     ap.add_argument("--num-units", type=int, default=0)
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--bf16-pv", action="store_true",
-                    help="two-token dense path: value product with bf16 P and V (MLA_FLAG_BF16_PV)")
+    ap.add_argument("--f16-pv", action="store_true",
+                    help="two-token dense path: value product with fp16 P and V (MLA_FLAG_F16_PV)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     args = ap.parse_args()

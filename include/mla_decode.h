@@ -75,10 +75,12 @@ enum {
   MLA_FLAG_CAUSAL = 1,   /* s_q = 2 MTP decode: token t sees [0, len - s_q + t] */
   MLA_FLAG_OUT_FP32 = 2, /* O is written as fp32 instead of bf16           */
   MLA_FLAG_VALIDATE = 4, /* check table / lengths / indices first (syncs)   */
-  MLA_FLAG_BF16_PV = 8   /* s_q = 2 dense only: the value product takes the
-                            softmax weights and values in bf16 (8 significant
-                            bits on the weights) instead of fp16 (11 bits);
-                            skips converting V; ignored elsewhere          */
+  MLA_FLAG_F16_PV = 8    /* s_q = 2 dense only: the value product takes the
+                            softmax weights and values in fp16 (11 significant
+                            bits on the weights) instead of bf16 (8 bits);
+                            V must then stay below 65504 in magnitude and is
+                            converted in shared memory (slower); the s_q = 1
+                            and top-k paths always use fp16               */
 };
 
 enum { MLA_NUM_HEADS = 128, MLA_D_QK = 576, MLA_D_V = 512, MLA_PAGE = 64 };

@@ -240,7 +240,7 @@ int mla_decode(const void* q, const void* kv_cache, int64_t num_pages, const int
   if (!q || !kv_cache || !block_table || !cache_lens || !workspace || !out || !lse) return MLA_ERR_INVALID_ARG;
   if (batch < 1 || num_pages < 1 || bt_stride < 1 || topk < 0) return MLA_ERR_INVALID_ARG;
   if ((topk_idx == nullptr) != (topk == 0)) return MLA_ERR_INVALID_ARG;
-  if (flags & ~static_cast<unsigned>(MLA_FLAG_CAUSAL | MLA_FLAG_OUT_FP32 | MLA_FLAG_VALIDATE | MLA_FLAG_BF16_PV))
+  if (flags & ~static_cast<unsigned>(MLA_FLAG_CAUSAL | MLA_FLAG_OUT_FP32 | MLA_FLAG_VALIDATE | MLA_FLAG_F16_PV))
     return MLA_ERR_INVALID_ARG;
   if (num_heads != kHeads || s_q < 1 || s_q > 2) return MLA_ERR_UNSUPPORTED;
   if (!std::isfinite(softmax_scale) || !(softmax_scale > 0.f)) return MLA_ERR_INVALID_ARG;
@@ -312,7 +312,7 @@ int mla_decode(const void* q, const void* kv_cache, int64_t num_pages, const int
     const uint64_t rows = static_cast<uint64_t>(num_pages) * kPage;
     if ((rc = encode_kv_3d(&tm_k3, kv_cache, rows, 3)) != MLA_OK) return rc;
     if ((rc = encode_kv_3d(&tm_v2, kv_cache, rows, 2)) != MLA_OK) return rc;
-    e = mtp_launch((flags & MLA_FLAG_BF16_PV) != 0, U, s, p, tm_q, tm_k3, tm_v2);
+    e = mtp_launch((flags & MLA_FLAG_F16_PV) == 0, U, s, p, tm_q, tm_k3, tm_v2);
   } else {
     e = decode_launch(topk_idx != nullptr, U * s_q, s, p, tm_q, tm_kv);
   }
@@ -326,7 +326,7 @@ int mla_decode(const void* q, const void* kv_cache, int64_t num_pages, const int
 int mla_combine(void* workspace, size_t ws_bytes, int batch, int s_q, int num_heads, unsigned flags,
                 int num_units, void* out, float* lse, mla_stream_t stream) {
   if (!workspace || !out || !lse || batch < 1) return MLA_ERR_INVALID_ARG;
-  if (flags & ~static_cast<unsigned>(MLA_FLAG_CAUSAL | MLA_FLAG_OUT_FP32 | MLA_FLAG_VALIDATE | MLA_FLAG_BF16_PV))
+  if (flags & ~static_cast<unsigned>(MLA_FLAG_CAUSAL | MLA_FLAG_OUT_FP32 | MLA_FLAG_VALIDATE | MLA_FLAG_F16_PV))
     return MLA_ERR_INVALID_ARG;
   if (num_heads != kHeads || s_q < 1 || s_q > 2) return MLA_ERR_UNSUPPORTED;
   if (!aligned(out, 16) || !aligned(lse, 4) || !aligned(workspace, 256)) return MLA_ERR_INVALID_ARG;

@@ -10,6 +10,7 @@
 namespace mla {
 
 // ------------------------------------------------------------------ plan
+constexpr int kPlanSmemReqs = 4096;  // requests whose cost prefix the plan keeps in shared memory
 // Block-wide inclusive scan of one int per thread (1024 threads).
 __device__ int block_inclusive_scan(int v, int* s_warp, int& total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -38,11 +39,15 @@ __device__ int block_inclusive_scan(int v, int* s_warp, int& total) {
 
 // One CTA of 1024 threads.  Step 1: tiles and cost prefix per request.
 // Step 2: split count and first partial slot per request.  Step 3: the
-// (request, tile) range of every unit.  Also resets the status word.
+// (request, tile) range of every unit, by binary search over the cost
+// prefixes (kept in shared memory when they fit: the searches are chains of
+// dependent reads).  Also resets the status word.
 __global__ void __launch_bounds__(1024) mla_plan_kernel(const int* __restrict__ lens, int B, int topk,
                                                         int tile_rows, int U, int* hdr, int* unit_meta,
                                                         int* req_meta, int slots_cap) {
   __shared__ int s_warp[32];
+  __shared__ int s_prefix[kPlanSmemReqs];
+  const bool prefix_in_smem = B <= kPlanSmemReqs;
   int carry = 0, tot = 0;
   for (int base = 0; base < B; base += blockDim.x) {
     const int b = base + threadIdx.x;
@@ -52,6 +57,7 @@ __global__ void __launch_bounds__(1024) mla_plan_kernel(const int* __restrict__ 
     if (b < B) {
       req_meta[4 * b + 0] = n;
       req_meta[4 * b + 3] = carry + incl - c;
+      if (prefix_in_smem) s_prefix[b] = carry + incl - c;
     }
     carry += tot;
   }
@@ -72,7 +78,7 @@ __global__ void __launch_bounds__(1024) mla_plan_kernel(const int* __restrict__ 
     carry += tot;
   }
   __syncthreads();
-  auto prefix = [&](int b) { return req_meta[4 * b + 3]; };
+  auto prefix = [&](int b) { return prefix_in_smem ? s_prefix[b] : req_meta[4 * b + 3]; };
   for (int u = threadIdx.x; u < U; u += blockDim.x) {
     const UnitInfo ui = plan_unit(u, W, total, B, prefix);
     int* m = unit_meta + 5 * u;

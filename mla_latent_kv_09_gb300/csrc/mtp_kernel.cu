@@ -33,8 +33,9 @@
 // soon as the score MMAs reading them finish, a page slot as soon as the value
 // MMAs of that page finish.  The MMA thread waits once per slot group: a wait
 // costs about 170 cycles of issue time, which a group's 12 queued MMAs hide.
-// P and V are fp16 (11 significant bits on the softmax weights; values must
-// stay below 65504 in magnitude), or bf16 in the kBf16PV variant.
+// P and V are bf16 (the kBf16PV variant, the default), or fp16 on request
+// (11 significant bits on the softmax weights instead of 8; values must then
+// stay below 65504 in magnitude, and V is converted in shared memory).
 //
 // Warps (640 threads).  Score ranks: 0-15 softmax (warp w: head rows
 // 32 (w % 4) .., key columns 32 (w / 4) .. of each tile), 16 and 19 MMA issue
@@ -46,11 +47,12 @@
 // Two threads issue the score MMAs, alternating tiles: a single issuing
 // thread leaves the tensor pipe idle while it waits on a barrier (a wait is
 // ~150 cycles even when the barrier is complete, and the MMA queue holds
-// little more than one MMA).  Each issuer does all the waits of its tile
-// (score buffer free, three slot groups landed) while the other issues, then
-// takes an issue token from the other and issues its 36 MMAs without a wait,
-// passing the token on after 24 of them.  Tiles thus follow each other in
-// the pipe, which keeps the chunk ring's full lookahead.
+// little more than one MMA).  Each issuer waits for its tile's score buffer
+// and first slot group while the other issues, then takes an issue token from
+// the other and issues its 36 MMAs, waiting for the two later slot groups
+// between them (their loads started only as the tile two back freed its
+// groups), and passes the token on after 24 MMAs.  Tiles thus follow each
+// other in the pipe, which keeps the chunk ring's full lookahead.
 //
 // P travels as one bulk copy per tile: the softmax warps write it into a
 // local copy laid out as the value rank's A operand; the shipper warp sends
@@ -316,9 +318,8 @@ mla_decode_mtp_kernel(const __grid_constant__ DecodeParams p, const __grid_const
         const uint32_t sb = g & 1u, ph = (g >> 1) & 1u;
         if (sb != own) continue;
         if (!(ok = wait_bar<true>(bar(kSE + sb), ph ^ 1u, ctl))) break;
-        for (uint32_t G = u / kKGroup; G < (u + kNumChunks) / kKGroup && ok; ++G)
-          ok = wait_bar<true>(kf0 + 8u * (G % kKGroups), (G / kKGroups) & 1u, ctl);
-        if (!ok) break;
+        if (!(ok = wait_bar<true>(kf0 + 8u * ((u / kKGroup) % kKGroups), ((u / kKGroup) / kKGroups) & 1u, ctl)))
+          break;
         if (g > 0 && !(ok = wait_bar<false>(bar(kHand + ((g - 1u) & 1u)), ((g - 1u) >> 1) & 1u, ctl))) break;
         tc_fence_after();
         const uint32_t dS = tmem + kColS + 128u * sb;
@@ -328,6 +329,10 @@ mla_decode_mtp_kernel(const __grid_constant__ DecodeParams p, const __grid_const
           const uint32_t uc = u + c;
           const uint32_t G = uc / kKGroup;
           if (c == 6) mbar_arrive_relaxed(bar(kHand + sb));  // the other issuer may start its tile
+          if (c > 0 && c % kKGroup == 0) {  // the next slot group (the first was waited for above)
+            if (!(ok = wait_bar<true>(kf0 + 8u * (G % kKGroups), (G / kKGroups) & 1u, ctl))) break;
+            tc_fence_after();
+          }
           const uint64_t bd = smem_desc(slot0 + (uc % kKSlots) * kPageChunk, 16u, 1024u);
           if (c < 8) {
 #pragma unroll

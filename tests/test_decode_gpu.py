@@ -31,11 +31,11 @@ def _build():
 
 
 def run(w, out_fp32=True, num_units=0, validate=False, q=None, kv=None, table=None, topk_idx="same",
-        bf16_pv=False):
+        f16_pv=False):
     o, lse = m.decode_step(w.q if q is None else q, w.kv if kv is None else kv,
                            w.block_table if table is None else table, w.cache_lens, w.softmax_scale,
                            causal=w.causal, topk_idx=w.topk_idx if topk_idx == "same" else topk_idx,
-                           out_fp32=out_fp32, num_units=num_units, validate=validate, bf16_pv=bf16_pv)
+                           out_fp32=out_fp32, num_units=num_units, validate=validate, f16_pv=f16_pv)
     torch.cuda.synchronize()
     return o.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64)
 
@@ -181,20 +181,20 @@ def test_two_token_lengths_around_tile_edges(L, causal):
     assert_close(o, lse, o_ref, lse_ref)
 
 
-@pytest.mark.parametrize("bf16_pv", [False, True], ids=["f16pv", "bf16pv"])
-def test_two_token_value_precision_modes(bf16_pv):
+@pytest.mark.parametrize("f16_pv", [False, True], ids=["bf16pv", "f16pv"])
+def test_two_token_value_precision_modes(f16_pv):
     w = wl.make_config("mtp_b64", device="cuda", batch=6, length=3000)
     o_ref, lse_ref = reference(w)
-    o, lse = run(w, bf16_pv=bf16_pv)
+    o, lse = run(w, f16_pv=f16_pv)
     assert_close(o, lse, o_ref, lse_ref)
-    ob, _ = run(w, out_fp32=False, bf16_pv=bf16_pv)
+    ob, _ = run(w, out_fp32=False, f16_pv=f16_pv)
     assert_close(ob, lse, o_ref, lse_ref)
 
 
-def test_two_token_full_size_bf16_pv_sampled():
+def test_two_token_full_size_f16_pv_sampled():
     w = wl.make_config("mtp_b64", device="cuda")
     sel = [(b, t) for b in (3, 17, 40, 63) for t in range(2)]
-    o, lse = run(w, bf16_pv=True)
+    o, lse = run(w, f16_pv=True)
     o_ref, lse_ref = reference(w, select=sel)
     assert_close(o, lse, o_ref, lse_ref, select=sel)
 
