@@ -29,7 +29,16 @@ sys.path.insert(0, ROOT)
 
 METRIC = "MLA decode us/call, TFLOPS and HBM GB/s as % of GB300 roofline (B=64)"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-DECODE_SOURCES = ["decode_kernel.cu", "ptx.cuh", "common.cuh", "plan.cuh"]
+COMMON_SOURCES = ["ptx.cuh", "common.cuh", "kernel_common.cuh", "plan.cuh"]
+
+
+TWO_TOKEN_DENSE = {"mtp_b64"}  # workloads with s_q = 2 and no top-k lists
+
+
+def kernel_sources(workload: str):
+    """Sources of the attention kernel a workload runs: two-token dense
+    requests take the paired-SM kernel, everything else the one-token one."""
+    return (["mtp_kernel.cu"] if workload in TWO_TOKEN_DENSE else ["decode_kernel.cu"]) + COMMON_SOURCES
 
 
 def peaks():
@@ -40,9 +49,9 @@ def peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_hash() -> str:
+def kernel_hash(workload: str) -> str:
     h = hashlib.sha256()
-    for f in DECODE_SOURCES:
+    for f in kernel_sources(workload):
         h.update(open(os.path.join(ROOT, "mla_latent_kv_09_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
@@ -55,7 +64,7 @@ def measured_traffic(workload: str):
         return None
     d = json.load(open(path))
     e = d.get(workload)
-    if not e or e.get("kernel_hash") != kernel_hash():
+    if not e or e.get("kernel_hash") != kernel_hash(workload):
         return None
     return e.get("dram_bytes_per_launch")
 
