@@ -30,7 +30,8 @@ cudaError_t decode_launch(bool sparse, int num_clusters, cudaStream_t stream, co
 cudaError_t mtp_set_attrs();
 cudaError_t mtp_max_clusters(int* n, int num_clusters_hint);
 cudaError_t mtp_launch(bool bf16_pv, int num_clusters, cudaStream_t stream, const DecodeParams& p,
-                       const CUtensorMap& tm_q, const CUtensorMap& tm_k3, const CUtensorMap& tm_v2);
+                       const CUtensorMap& tm_q, const CUtensorMap& tm_k3, const CUtensorMap& tm_v2,
+                       const CUtensorMap& tm_out, const CUtensorMap& tm_part);
 }  // namespace mla
 
 using namespace mla;
@@ -154,6 +155,22 @@ int encode_kv_3d(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_c
   const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
                         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MLA_OK : MLA_ERR_CUDA;
+}
+
+// An output tensor of 512 columns per row (bf16 or fp32) for tensor stores of
+// 32-row boxes of 64-byte rows (32 bf16 or 16 fp32 columns), staged with the
+// 64-byte swizzle as the two-token kernel writes them.
+int encode_out_2d(CUtensorMap* m, void* base, uint64_t rows, bool fp32) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return MLA_ERR_CUDA;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kDv), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kDv) * (fp32 ? 4 : 2)};
+  const cuuint32_t box[2] = {fp32 ? 16u : 32u, 32u};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base,
+                        dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                        CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? MLA_OK : MLA_ERR_CUDA;
 }
 
@@ -312,7 +329,12 @@ int mla_decode(const void* q, const void* kv_cache, int64_t num_pages, const int
     const uint64_t rows = static_cast<uint64_t>(num_pages) * kPage;
     if ((rc = encode_kv_3d(&tm_k3, kv_cache, rows, 3)) != MLA_OK) return rc;
     if ((rc = encode_kv_3d(&tm_v2, kv_cache, rows, 2)) != MLA_OK) return rc;
-    e = mtp_launch((flags & MLA_FLAG_F16_PV) == 0, U, s, p, tm_q, tm_k3, tm_v2);
+    CUtensorMap tm_out, tm_part;  // O (bf16 or fp32) and the fp32 partials, for the epilogue's tensor stores
+    if ((rc = encode_out_2d(&tm_out, out, static_cast<uint64_t>(batch) * s_q * kHeads, p.out_fp32 != 0)) != MLA_OK)
+      return rc;
+    if ((rc = encode_out_2d(&tm_part, p.part_o, static_cast<uint64_t>(L.slots) * s_q * kHeads, true)) != MLA_OK)
+      return rc;
+    e = mtp_launch((flags & MLA_FLAG_F16_PV) == 0, U, s, p, tm_q, tm_k3, tm_v2, tm_out, tm_part);
   } else {
     e = decode_launch(topk_idx != nullptr, U * s_q, s, p, tm_q, tm_kv);
   }

@@ -73,7 +73,7 @@ namespace mtp {
 
 constexpr int kTileRows = 2 * kPage;              // 128 cached rows per tile
 constexpr int kPageChunk = kPage * 128;           // 8 KiB: 64 rows x 64 dims (bf16), 128B-swizzled
-constexpr int kKSlots = 18;                       // score ranks: chunk slots (two pages)
+constexpr int kKSlots = 21;                       // score ranks: chunk slots (2 1/3 tiles)
 constexpr int kKGroup = 3;                        // chunk slots per landing / free barrier
 constexpr int kKGroups = kKSlots / kKGroup;
 constexpr int kVPage = 4 * kPageChunk;            // 32 KiB: one page, this rank's 256 value dims
@@ -90,12 +90,12 @@ constexpr int kQChunk = kHeads * 128;             // 16 KiB: 128 heads x 64 dims
 // Shared memory (offsets from a 1024-aligned base; the barrier block sits at
 // the same offset in all four CTAs, which multicast commits rely on).
 constexpr int kOffStage = 0;                         // chunk slots (score ranks) / page slots (value ranks)
-constexpr int kOffQr = kKSlots * kPageChunk;         // score ranks: [2] Q dims 512..575
-constexpr int kOffXchg = kOffQr + 2 * kQChunk;       // score ranks: row max / sum exchange, 6 KiB
+constexpr int kOffQr = kKSlots * kPageChunk;         // score ranks: Q dims 512..575
+constexpr int kOffXchg = kOffQr + kQChunk;           // score ranks: row max / sum exchange, 6 KiB
 constexpr int kOffPs = kOffXchg + 6144;              // score ranks: outgoing P tile (same layout as kOffP)
 constexpr int kOffAlphaS = kOffPs + kPSlot;          // score ranks: outgoing float[128] rescale factors
 constexpr int kOffFinS = kOffAlphaS + kHeads * 4;    // score ranks: outgoing float[128] final scales
-constexpr int kEndS = kOffFinS + kHeads * 4;         // 201728
+constexpr int kEndS = kOffFinS + kHeads * 4;         // 228352
 constexpr int kOffP = kVSlots * kVPage;              // value ranks: [2] P tiles
 constexpr int kOffAlpha = kOffP + 2 * kPSlot;        // value ranks: float[2][128]
 constexpr int kOffFin = kOffAlpha + 2 * kHeads * 4;  // value ranks: float[2][128]
@@ -120,21 +120,21 @@ constexpr int kTmaWarp = 17;
 constexpr int kShipWarp = 18;                    // score ranks: P shipper
 constexpr int kMma2Warp = 19;                    // rank 0: issues the score MMAs of odd tiles
 constexpr float kRescaleLog2 = 8.0f;
-constexpr int kL2Ahead = 3;  // score ranks: tiles whose page is prefetched into L2 ahead of the ring
 
 constexpr uint16_t kScoreMask = 0x3;  // ranks 0, 1
 constexpr uint16_t kValueMask = 0xC;  // ranks 2, 3
 
 enum Bar {
-  kKF = 0,        // [6] rank 0: slot group landed in both score ranks (1 arrival + TMA tx of both)
-  kKE = 6,        // [6] score ranks: slot group free (commit from rank 0)
-  kQRF = 12,      // [2] rank 0: Q RoPE buffer landed in both score ranks (TMA tx of both)
-  kQFree = 14,    // [2] score ranks: both issuers' score MMAs of the segment using that RoPE buffer finished
+  kKF = 0,        // [7] rank 0: slot group landed in both score ranks (1 arrival + TMA tx of both)
+  kKE = 8,        // [7] score ranks: slot group free (commit from rank 0)
+  kQRF = 16,      // rank 0: Q RoPE part landed in both score ranks (TMA tx of both)
+  kQFree = 17,    // score ranks: both issuers' score MMAs of the segment finished (RoPE part may be replaced)
   kQF = 36,       // rank 0: both issuers' score MMAs of a segment finished (Q may be replaced)
   kQC = 37,       // rank 0: Q of the segment copied into tensor memory (commit from the first issuer)
   kSF = 38,       // [2] score ranks: scores ready (commit from rank 0)
-  kSE = 40,       // [2] rank 0: scores read (one arrival per row quarter of both ranks)
-  kPFree = 42,    // [2] score ranks: PV finished with that P slot (commit from rank 2)
+  kSE = 40,       // [2] rank 0: scores read (one arrival per softmax warp of both ranks)
+  kPFree = 42,    // [2] score ranks: the value rank is done with that P slot (commit from rank 2 after
+                  //     PV; after a segment's last tile, an arrival from the epilogue that staged O there)
   kVF = 44,       // [4] value ranks: page slot landed (TMA tx)
   kVE = 48,       // [4] value ranks: page slot free (commit from rank 2)
   kVR = 52,       // [4] rank 2: page slot converted in both value ranks
@@ -149,9 +149,30 @@ enum Bar {
   kMmaDone2 = 67, // teardown (second issuer)
   kHand = 68,     // [2] rank 0: score-MMA issue token (tile parity): the issuer of tile g may start
                   //     once the issuer of tile g - 1 has issued two thirds of its MMAs
-  kNumBars = 70
+  kEpiD = 70,     // value ranks: the conversion warps' share of a segment epilogue is written
+  kNumBars = 71
 };
 static_assert(kNumBars * 8 + 16 <= kBarBytes, "barrier block");
+static_assert(kKGroups <= kKE - kKF && kKGroups <= kQRF - kKE, "slot-group barriers");
+
+// Per segment the chunk ring carries pads, 16 Q halves (eight 16 KiB chunks,
+// each two adjacent slots), then 9 K chunks per tile.  A segment starts on a
+// group boundary u; q_pads(u) pads are inserted so that every Q chunk sits in
+// two adjacent slots (none straddles the ring's end) and the tiles that
+// follow start on a group boundary again.
+__host__ __device__ constexpr uint32_t q_pads(uint32_t u) {
+  return (u % kKSlots == 6u || u % kKSlots == 12u || u % kKSlots == 18u) ? 5u : 2u;
+}
+__host__ __device__ constexpr bool q_pads_ok() {
+  for (uint32_t r = 0; r < kKSlots; r += kKGroup) {
+    const uint32_t uq = r + q_pads(r);
+    if ((uq + 16u) % kKGroup != 0u) return false;
+    for (uint32_t i = 0; i < 8u; ++i)
+      if ((uq + 2u * i) % kKSlots == kKSlots - 1u) return false;
+  }
+  return true;
+}
+static_assert(kKSlots % kKGroup == 0 && q_pads_ok(), "Q chunks stay contiguous; tiles stay group-aligned");
 
 // kind::f16 instruction descriptors.  Scores: bf16 operands, M = 256, N = 128,
 // B (the cached rows) K-major.  Values: fp16 or bf16 operands (A and B of
@@ -184,7 +205,8 @@ __host__ __device__ constexpr uint32_t p_message_bytes(bool last) {
 template <bool kBf16PV>
 __global__ void __launch_bounds__(kThreads, 1)
 mla_decode_mtp_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tm_q,
-                      const __grid_constant__ CUtensorMap tm_k3, const __grid_constant__ CUtensorMap tm_v2) {
+                      const __grid_constant__ CUtensorMap tm_k3, const __grid_constant__ CUtensorMap tm_v2,
+                      const __grid_constant__ CUtensorMap tm_out, const __grid_constant__ CUtensorMap tm_part) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t mis = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* smem = smem_raw + mis;
@@ -216,10 +238,8 @@ mla_decode_mtp_kernel(const __grid_constant__ DecodeParams p, const __grid_const
       mbar_init(bar(kKF + i), 1);
       mbar_init(bar(kKE + i), 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(kQRF + i), 1);
-      mbar_init(bar(kQFree + i), 2);
-    }
+    mbar_init(bar(kQRF), 1);
+    mbar_init(bar(kQFree), 2);
     mbar_init(bar(kQC), 1);
     mbar_init(bar(kMmaDone2), 1);
     mbar_init(bar(kHand), 1);
@@ -231,7 +251,7 @@ mla_decode_mtp_kernel(const __grid_constant__ DecodeParams p, const __grid_const
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(kSF + i), 1);
-      mbar_init(bar(kSE + i), 8);
+      mbar_init(bar(kSE + i), 2 * kSoftmaxWarps);
       mbar_init(bar(kPFree + i), 1);
       mbar_init(bar(kPM + i), 1);
       mbar_init(bar(kPR + i), 2);
@@ -243,6 +263,7 @@ mla_decode_mtp_kernel(const __grid_constant__ DecodeParams p, const __grid_const
     mbar_init(bar(kMmaDone), 1);
     mbar_init(bar(kPsFull), kSoftmaxWarps);
     mbar_init(bar(kPsFree), 1);
+    mbar_init(bar(kEpiD), 1);
     misc[1] = 0u;
     fence_mbar_init();
   }
@@ -253,6 +274,10 @@ mla_decode_mtp_kernel(const __grid_constant__ DecodeParams p, const __grid_const
   if (warp == kTmaWarp && lane == 0) {
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(score_rank ? &tm_k3 : &tm_v2);
+    if (!score_rank) {
+      tma_prefetch_desc(&tm_out);
+      tma_prefetch_desc(&tm_part);
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -285,7 +310,7 @@ mla_decode_mtp_kernel(const __grid_constant__ DecodeParams p, const __grid_const
     const uint32_t kf0 = bar(kKF), ke0 = bar(kKE), slot0 = sbase + kOffStage;
     const uint32_t own = is_a ? 0u : 1u;
     while (ok && it.next(sg)) {
-      const uint32_t u_q = u + ((u % 6u == 0u) ? 2u : 5u);
+      const uint32_t u_q = u + q_pads(u);
       const uint32_t u_t = u_q + 16u;  // first use of the segment's tiles (a group boundary)
       if (is_a) {
         if (nseg > 0 && !(ok = wait_bar<false>(bar(kQF), (nseg - 1u) & 1u, ctl))) break;
@@ -312,8 +337,8 @@ mla_decode_mtp_kernel(const __grid_constant__ DecodeParams p, const __grid_const
         tc_fence_after();
       }
       u = u_t;
-      if (!(ok = wait_bar<true>(bar(kQRF + (nseg & 1u)), (nseg >> 1) & 1u, ctl))) break;
-      const uint64_t qr0 = smem_desc(sbase + kOffQr + (nseg & 1u) * kQChunk, 16u, 1024u);
+      if (!(ok = wait_bar<true>(bar(kQRF), nseg & 1u, ctl))) break;
+      const uint64_t qr0 = smem_desc(sbase + kOffQr, 16u, 1024u);
       for (int j = sg.t0; j < sg.t1 && ok; ++j, ++g, u += kNumChunks) {
         const uint32_t sb = g & 1u, ph = (g >> 1) & 1u;
         if (sb != own) continue;
@@ -353,12 +378,69 @@ mla_decode_mtp_kernel(const __grid_constant__ DecodeParams p, const __grid_const
       if (!ok) break;
       // this issuer's score MMAs of the segment: Q and the RoPE buffer may be replaced after both
       umma_commit_pair(bar(kQF), 1u << 0);
-      umma_commit_pair(bar(kQFree + (nseg & 1u)), kScoreMask);
+      umma_commit_pair(bar(kQFree), kScoreMask);
       ++nseg;
     }
     const uint32_t done = bar(is_a ? kMmaDone : kMmaDone2);
     umma_commit_pair(done, 1u << 0);  // every MMA this thread issued has finished
     drain_bar(done, 0);
+  };
+
+  // ======================================================= segment epilogue share
+  // Warp w (0-15) of a value rank writes rows 32 (w % 4) .. +31 (its
+  // tensor-memory lane quarter), columns 128 (w / 4) .. +127 of O times
+  // `fin`: 32-row boxes of 64-byte rows (32 bf16 or 16 fp32 columns) staged
+  // with the 64-byte swizzle in the warp's 2 KiB of P slot `pb` (free: PV has
+  // finished with it, and the score rank refills it only after the epilogue)
+  // and written by tensor stores, so both the shared-memory writes and the
+  // global writes are full-width.
+  auto epilogue_share = [&](int w, float fin, const Seg& sg, uint32_t pb) {
+    const bool to_part = sg.slot >= 0;
+    if (to_part && sg.slot >= 2 * U) return;  // the plan never uses more than 2 * (U - 1) slots
+    const bool f32 = to_part || p.out_fp32;
+    const CUtensorMap* tm = to_part ? &tm_part : &tm_out;
+    const long long orow = to_part ? static_cast<long long>(sg.slot) * 2 + tok : static_cast<long long>(sg.b) * 2 + tok;
+    const int y = static_cast<int>(orow * kHeads) + 32 * (w & 3);
+    const int x0 = 128 * (w >> 2);
+    const uint32_t ul = static_cast<uint32_t>(lane);
+    const uint32_t stg = sbase + kOffP + pb * kPSlot + static_cast<uint32_t>(w) * 2048u;
+    const uint32_t srow = stg + ul * 64u, sw = (ul >> 1) & 3u;
+    const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * (w & 3)) << 16) + kColO + static_cast<uint32_t>(x0);
+    const int nbox = f32 ? 8 : 4, bw = f32 ? 16 : 32;
+#pragma unroll 1
+    for (int i = 0; i < nbox; ++i) {
+      uint32_t v[16];
+      if (f32) {
+        uint32_t r[16];
+        tmem_ld16(taddr + static_cast<uint32_t>(16 * i), r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 16; ++c) v[c] = __float_as_uint(__uint_as_float(r[c]) * fin);
+      } else {
+        uint32_t r[32];
+        tmem_ld32(taddr + static_cast<uint32_t>(32 * i), r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+          v[c] = pack_bf16x2(__uint_as_float(r[2 * c]) * fin, __uint_as_float(r[2 * c + 1]) * fin);
+      }
+      if (i > 0) {  // the previous box's store has read the staging
+        if (lane == 0) bulk_wait_read();
+        __syncwarp();
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        st_shared_v4(srow + ((static_cast<uint32_t>(k) ^ sw) << 4), v[4 * k], v[4 * k + 1], v[4 * k + 2],
+                     v[4 * k + 3]);
+      fence_proxy_async_smem();  // generic writes, read next by the tensor store
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(tm, stg, x0 + bw * i, y);
+        bulk_commit();
+      }
+    }
+    if (lane == 0) bulk_wait_read();
+    __syncwarp();
   };
 
   if (score_rank && warp < kSoftmaxWarps) {
@@ -402,9 +484,12 @@ mla_decode_mtp_kernel(const __grid_constant__ DecodeParams p, const __grid_const
           uint32_t r[32];
           tmem_ld32(tmem + lane_base + kColS + 128u * sb + 32u * cg, r);
           tmem_wait_ld();
+          tc_fence_before();
+          // this warp has read its scores: the buffer's next tile may start
+          // as soon as all 32 softmax warps of the pair have
+          if (lane == 0) mbar_arrive_remote_relaxed(rSE + 8u * sb);
 #pragma unroll
           for (int c = 0; c < 32; ++c) s[c] = __uint_as_float(r[c]);
-          tc_fence_before();
         } else {
 #pragma unroll
           for (int c = 0; c < 32; ++c) s[c] = NEG_INF;
@@ -426,8 +511,6 @@ mla_decode_mtp_kernel(const __grid_constant__ DecodeParams p, const __grid_const
           stop = true;
           break;
         }
-        // the quarter has read its scores (tcgen05.wait::ld completed the reads)
-        if (lead && lane == 0) mbar_arrive_remote_relaxed(rSE + 8u * sb);
         const float* xm = xmax + sb * 4 * kHeads + row;
         const float mt = fmaxf(fmaxf(xm[0], xm[kHeads]), fmaxf(xm[2 * kHeads], xm[3 * kHeads])) * p.scale_log2;
 
@@ -523,6 +606,7 @@ mla_decode_mtp_kernel(const __grid_constant__ DecodeParams p, const __grid_const
     const volatile float* fin_s = reinterpret_cast<const volatile float*>(smem + kOffFin);
     const uint32_t rPR = mapa(bar(kPR), 2);
     const uint32_t rOE = mapa(bar(kOE), 2);
+    const uint32_t rPFree = mapa(bar(kPFree), tok);  // the score rank that ships this rank's P
     SegIter it(p, unit);
     Seg sg;
     uint32_t g = 0, nseg = 0;
@@ -564,55 +648,35 @@ mla_decode_mtp_kernel(const __grid_constant__ DecodeParams p, const __grid_const
           stop = true;
           break;
         }
-        if (row == 0) mbar_arrive_remote(rPR + 8u * pb);
+        // relaxed: what it hands over is P, whose landing this CTA observed on
+        // its own barrier, and O rows whose rescale tcgen05.wait::st completed;
+        // a release arrive would first wait for this thread's earlier memory
+        // operations, a thousand cycles on the path of every tile
+        if (row == 0) mbar_arrive_remote_relaxed(rPR + 8u * pb);
 
-        if (last) {  // ---- segment epilogue: O * fin -> global
+        if (last) {  // ---- segment epilogue: O * fin -> global, shared with the conversion warps
           ok = warp_wait(bar(kOF), nseg & 1u, ctl);
           if (!named_bar_all(5, 128, ok)) {
             stop = true;
             break;
           }
           tc_fence_after();
-          const long long bt_row = static_cast<long long>(sg.b) * 2 + tok;
-          if (sg.slot < 0 && !p.out_fp32) {
-            uint16_t* dst0 = static_cast<uint16_t*>(p.out) + (bt_row * kHeads + row) * kDv;
-#pragma unroll 1
-            for (int cc = 0; cc < 16; ++cc) {
-              uint32_t r[32];
-              tmem_ld32(tmem + lane_base + kColO + 32u * cc, r);
-              tmem_wait_ld();
-              uint4* dst = reinterpret_cast<uint4*>(dst0 + 32 * cc);
-#pragma unroll
-              for (int k = 0; k < 4; ++k)
-                dst[k] = make_uint4(
-                    pack_bf16x2(__uint_as_float(r[8 * k + 0]) * fin, __uint_as_float(r[8 * k + 1]) * fin),
-                    pack_bf16x2(__uint_as_float(r[8 * k + 2]) * fin, __uint_as_float(r[8 * k + 3]) * fin),
-                    pack_bf16x2(__uint_as_float(r[8 * k + 4]) * fin, __uint_as_float(r[8 * k + 5]) * fin),
-                    pack_bf16x2(__uint_as_float(r[8 * k + 6]) * fin, __uint_as_float(r[8 * k + 7]) * fin));
-            }
-          } else if (sg.slot < 2 * U) {
-            float* dst0 = sg.slot < 0
-                ? static_cast<float*>(p.out) + (bt_row * kHeads + row) * kDv
-                : p.part_o + ((static_cast<long long>(sg.slot) * 2 + tok) * kHeads + row) * kDv;
-#pragma unroll 1
-            for (int cc = 0; cc < 16; ++cc) {
-              uint32_t r[32];
-              tmem_ld32(tmem + lane_base + kColO + 32u * cc, r);
-              tmem_wait_ld();
-              float4* dst = reinterpret_cast<float4*>(dst0 + 32 * cc);
-#pragma unroll
-              for (int k = 0; k < 8; ++k)
-                dst[k] = make_float4(__uint_as_float(r[4 * k]) * fin, __uint_as_float(r[4 * k + 1]) * fin,
-                                     __uint_as_float(r[4 * k + 2]) * fin, __uint_as_float(r[4 * k + 3]) * fin);
-            }
-          }
+          epilogue_share(warp, fin, sg, pb);
+          ok = warp_wait(bar(kEpiD), nseg & 1u, ctl);  // the other twelve warps' shares
           tc_fence_before();
-          named_bar_sync(5, 128);
-          if (row == 0) mbar_arrive_remote_relaxed(rOE);  // O read (tcgen05.wait::ld completed)
+          if (!named_bar_all(5, 128, ok)) {
+            stop = true;
+            break;
+          }
+          if (row == 0) {
+            mbar_arrive_remote_relaxed(rOE);       // O read (tcgen05.wait::ld completed in all 16 warps)
+            mbar_arrive_remote(rPFree + 8u * pb);  // the staging (this P slot) is free again
+          }
         }
       }
       ++nseg;
     }
+    if (lane == 0) bulk_wait_all();  // the output stores have completed
   } else if (warp == kMmaWarp || warp == kMma2Warp) {
     // ================================================= MMA issue (rank 0: two threads, rank 2: one)
     if (lane == 0 && rank == 0) {
@@ -649,7 +713,9 @@ mla_decode_mtp_kernel(const __grid_constant__ DecodeParams p, const __grid_const
             umma_commit_pair(bar(kVE + rv.idx), kValueMask);
           }
           if (!ok) break;
-          umma_commit_pair(bar(kPFree + pb), kScoreMask);  // the score ranks may reuse this P slot
+          // the score ranks may reuse this P slot (after a segment's last tile the
+          // epilogue stages O there and frees it)
+          if (j != sg.t1 - 1) umma_commit_pair(bar(kPFree + pb), kScoreMask);
           umma_commit_pair(bar(kPD + pb), kValueMask);
           if (j == sg.t1 - 1) umma_commit_pair(bar(kOF), kValueMask);
         }
@@ -670,8 +736,8 @@ mla_decode_mtp_kernel(const __grid_constant__ DecodeParams p, const __grid_const
     if (score_rank) {
       // Both score ranks fill their own chunk slots; every copy completes on
       // rank 0's barriers, which rank 0 arms with the bytes of both.  The use
-      // sequence is the issuers': per segment 2 or 5 pads, 16 Q halves, then
-      // 9 K chunks per tile.
+      // sequence is the issuers': per segment q_pads() pads, 16 Q halves,
+      // then 9 K chunks per tile.
       const uint32_t rKF = mapa(bar(kKF), 0);
       const uint32_t rQRF = mapa(bar(kQRF), 0);
       uint32_t u = 0, nseg = 0;
@@ -692,15 +758,7 @@ mla_decode_mtp_kernel(const __grid_constant__ DecodeParams p, const __grid_const
       while (ok && it.next(sg)) {
         const int L = max(p.cache_lens[sg.b], 0);
         const int qy = (sg.b * 2 + static_cast<int>(tok)) * kHeads;
-        // RoPE part of Q into buffer nseg % 2 once segment nseg - 2 is done with it
-        if (nseg >= 2 && !(ok = warp_wait(bar(kQFree + (nseg & 1u)), ((nseg - 2u) >> 1) & 1u, ctl))) break;
-        if (lane == 0) {
-          if (tok == 0) mbar_arrive_expect_tx_relaxed(bar(kQRF + (nseg & 1u)), 2u * kQChunk);
-          for (int h = 0; h < 2; ++h)
-            tma_load_2d_pair(sbase + kOffQr + (nseg & 1u) * kQChunk + h * kPageChunk, &tm_q, 8 * kChunk,
-                             qy + h * kPage, rQRF + 8u * (nseg & 1u));
-        }
-        for (uint32_t npad = (u % 6u == 0u) ? 2u : 5u; npad > 0 && ok; --npad) {  // pads
+        for (uint32_t npad = q_pads(u); npad > 0 && ok; --npad) {  // pads
           if (!(ok = claim(0))) break;
           ++u;
         }
@@ -714,6 +772,13 @@ mla_decode_mtp_kernel(const __grid_constant__ DecodeParams p, const __grid_const
           }
         }
         if (!ok) break;
+        // RoPE part of Q (not in the ring) once the previous segment's score MMAs are done with it
+        if (nseg >= 1 && !(ok = warp_wait(bar(kQFree), (nseg - 1u) & 1u, ctl))) break;
+        if (lane == 0) {
+          if (tok == 0) mbar_arrive_expect_tx_relaxed(bar(kQRF), 2u * kQChunk);
+          for (int h = 0; h < 2; ++h)
+            tma_load_2d_pair(sbase + kOffQr + h * kPageChunk, &tm_q, 8 * kChunk, qy + h * kPage, rQRF);
+        }
         const int* bt_row = p.block_table + static_cast<long long>(sg.b) * p.bt_stride;
         const int npages = (L + kPage - 1) / kPage;
         for (int jb = sg.t0; jb < sg.t1 && ok; jb += 32) {
@@ -724,15 +789,8 @@ mla_decode_mtp_kernel(const __grid_constant__ DecodeParams p, const __grid_const
             const int pg = bt_row[pi];
             my_page = (pg >= 0 && pg < p.num_pages) ? pg : -1;
           }
-          // the ring holds two tiles, less than the load latency under load:
-          // pages a few tiles ahead are pulled into L2 (no shared memory needed)
-          if (lane < kL2Ahead && lane < cnt && my_page >= 0)
-            bulk_prefetch_l2(p.kv + static_cast<long long>(my_page) * kPage * kDqk, kPage * kDqk * 2);
           for (int jj = 0; jj < cnt && ok; ++jj) {
             const int page = __shfl_sync(0xffffffffu, my_page, jj);
-            const int pf = __shfl_sync(0xffffffffu, my_page, min(jj + kL2Ahead, 31));
-            if (lane == 0 && jj + kL2Ahead < cnt && pf >= 0)
-              bulk_prefetch_l2(p.kv + static_cast<long long>(pf) * kPage * kDqk, kPage * kDqk * 2);
             const int y = page >= 0 ? page * kPage : static_cast<int>(p.num_pages) * kPage;
             // a tile is three whole slot groups: one 3-chunk load per group
             for (int c = 0; c < kNumChunks; c += kKGroup) {
@@ -803,13 +861,15 @@ mla_decode_mtp_kernel(const __grid_constant__ DecodeParams p, const __grid_const
     const int ptid = threadIdx.x - 128;
     const uint32_t rVR = mapa(bar(kVR), 2);
     constexpr int kPieces = kVPage / 16;  // 2048 pieces of 16 B
+    const volatile float* fin_s = reinterpret_cast<const volatile float*>(smem + kOffFin);
     SegIter it(p, unit);
     Seg sg;
     Ring<kVSlots> rv;
+    uint32_t g = 0, nseg = 0;
     bool stop = false;  // the twelve warps vote at every named barrier
     while (!stop && it.next(sg)) {
       const int L = max(p.cache_lens[sg.b], 0);
-      for (int j = sg.t0; j < sg.t1 && !stop; ++j) {
+      for (int j = sg.t0; j < sg.t1 && !stop; ++j, ++g) {
         for (int e = 0; e < 2; ++e, rv.advance()) {
           const bool ok = warp_wait(bar(kVF + rv.idx), rv.phase, ctl);
           if (!named_bar_all(6, kConvThreads, ok)) {
@@ -845,8 +905,24 @@ mla_decode_mtp_kernel(const __grid_constant__ DecodeParams p, const __grid_const
           named_bar_sync(6, kConvThreads);
           if (ptid == 0) mbar_arrive_remote(rVR + 8u * rv.idx);
         }
+        if (!stop && j == sg.t1 - 1) {  // ---- this group's share of the segment epilogue
+          const uint32_t pb = g & 1u;
+          // O complete; the last P message (with the final scales) landed
+          bool ok = warp_wait(bar(kOF), nseg & 1u, ctl) && warp_wait(bar(kPM + pb), (g >> 1) & 1u, ctl);
+          if (!named_bar_all(6, kConvThreads, ok)) {
+            stop = true;
+            break;
+          }
+          tc_fence_after();
+          epilogue_share(warp, fin_s[pb * kHeads + 32 * (warp & 3) + lane], sg, pb);
+          tc_fence_before();
+          named_bar_sync(6, kConvThreads);
+          if (ptid == 0) mbar_arrive(bar(kEpiD));
+        }
       }
+      ++nseg;
     }
+    if (lane == 0) bulk_wait_all();  // the output stores have completed
   }
 
   // ======================================================= teardown
@@ -894,12 +970,14 @@ cudaError_t mtp_max_clusters(int* n, int num_clusters_hint) {
 }
 
 cudaError_t mtp_launch(bool bf16_pv, int num_clusters, cudaStream_t stream, const DecodeParams& p,
-                       const CUtensorMap& tm_q, const CUtensorMap& tm_k3, const CUtensorMap& tm_v2) {
+                       const CUtensorMap& tm_q, const CUtensorMap& tm_k3, const CUtensorMap& tm_v2,
+                       const CUtensorMap& tm_out, const CUtensorMap& tm_part) {
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[1];
   mtp::cluster_config<false>(cfg, attr, num_clusters, stream);
-  return bf16_pv ? cudaLaunchKernelEx(&cfg, mtp::mla_decode_mtp_kernel<true>, p, tm_q, tm_k3, tm_v2)
-                 : cudaLaunchKernelEx(&cfg, mtp::mla_decode_mtp_kernel<false>, p, tm_q, tm_k3, tm_v2);
+  return bf16_pv
+      ? cudaLaunchKernelEx(&cfg, mtp::mla_decode_mtp_kernel<true>, p, tm_q, tm_k3, tm_v2, tm_out, tm_part)
+      : cudaLaunchKernelEx(&cfg, mtp::mla_decode_mtp_kernel<false>, p, tm_q, tm_k3, tm_v2, tm_out, tm_part);
 }
 
 }  // namespace mla
