@@ -242,15 +242,18 @@ def run_ours(args, world, rank, local):
     flags = (m.MLA_FLAG_CAUSAL if w.causal else 0) | (m.MLA_FLAG_F16_PV if args.f16_pv else 0)
     U = ws.num_units
 
+    # every call goes to the stream current at call time (the capture stream
+    # while a CUDA graph of the step is recorded)
     def plan():
-        m.mla_decode_plan(w.cache_lens, B, s_q, topk, U, ws.buf, ws.nbytes, stream)
+        m.mla_decode_plan(w.cache_lens, B, s_q, topk, U, ws.buf, ws.nbytes, torch.cuda.current_stream(dev))
 
     def decode():
         m.mla_decode(w.q, w.kv, w.num_pages, w.block_table, w.block_table.stride(0), w.cache_lens, B, s_q,
-                     128, w.softmax_scale, w.topk_idx, topk, flags, U, ws.buf, ws.nbytes, out, lse, stream)
+                     128, w.softmax_scale, w.topk_idx, topk, flags, U, ws.buf, ws.nbytes, out, lse,
+                     torch.cuda.current_stream(dev))
 
     def combine():
-        m.mla_combine(ws.buf, ws.nbytes, B, s_q, 128, flags, U, out, lse, stream)
+        m.mla_combine(ws.buf, ws.nbytes, B, s_q, 128, flags, U, out, lse, torch.cuda.current_stream(dev))
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -280,11 +283,49 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     barrier(world)
     wall = time.perf_counter() - t_wall
-    clocks = sampler.stop()
-    step_ms = sum(e[0].elapsed_time(e[3]) for e in ev) / args.steps
+    launch_ms = sum(e[0].elapsed_time(e[3]) for e in ev) / args.steps
     dec_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / args.steps
     plan_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps
     comb_ms = sum(e[2].elapsed_time(e[3]) for e in ev) / args.steps
+    step_ms = launch_ms
+    if not args.no_graph:
+        # the step as a serving loop runs it: plan + decode + combine recorded
+        # once in a CUDA graph (the decode and combine kernels are programmatic
+        # dependents of the kernel before them) and replayed; the loop above,
+        # with an event between kernels, gives the per-kernel split
+        ref_out, ref_lse = out.clone(), lse.clone()
+        graph = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            plan(); decode(); combine()
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(graph):
+            plan(); decode(); combine()
+        for _ in range(args.warmup):
+            flush.zero_()
+            graph.replay()
+        torch.cuda.synchronize()
+        evg = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+        barrier(world)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter()
+        for i in range(args.steps):
+            flush.zero_()
+            evg[i][0].record(stream)
+            graph.replay()
+            evg[i][1].record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        wall = time.perf_counter() - t_wall
+        step_ms = sum(e[0].elapsed_time(e[1]) for e in evg) / args.steps
+        status = m.mla_workspace_status(ws.buf, stream.cuda_stream)
+        if status != 0:
+            raise RuntimeError(f"device status after the graph replays: {m.mla_status_string(status)}")
+        if not (torch.equal(out, ref_out) and torch.equal(lse, ref_lse)):
+            raise RuntimeError("graph replays changed the output of the step")
+    clocks = sampler.stop()
     step_ms_max = max_over_ranks(step_ms, world)
     value = world * flops / (step_ms_max * 1e-3) / 1e12
 
@@ -342,6 +383,9 @@ def run_ours(args, world, rank, local):
                    "l2": "256 MB L2 flush before every timed step; cache pool exceeds L2",
                    "algorithmic_gflop": flops / 1e9, "algorithmic_mb": nbytes / 1e6},
         "us_per_call": step_ms_max * 1e3,
+        "launch": "CUDA graph of plan + decode + combine, replayed" if not args.no_graph
+                  else "plan, decode, combine launched from the host",
+        "us_per_call_host_launches": launch_ms * 1e3,
         "us_decode_kernel": dec_ms * 1e3, "us_plan": plan_ms * 1e3, "us_combine": comb_ms * 1e3,
         "tflops": flops / (step_ms * 1e-3) / 1e12,
         "hbm_gbs": nbytes / (step_ms * 1e-3) / 1e9,
@@ -373,6 +417,8 @@ def main():
     ap.add_argument("--num-units", type=int, default=0)
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="time the step from host launches instead of a CUDA graph replay")
     ap.add_argument("--f16-pv", action="store_true",
                     help="two-token dense path: value product with fp16 P and V (MLA_FLAG_F16_PV)")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -360,11 +360,26 @@ int mla_combine(void* workspace, size_t ws_bytes, int batch, int s_q, int num_he
   const WsLayout L = ws_layout(batch, s_q, U);
   if (ws_bytes < L.total) return MLA_ERR_WORKSPACE;
   const char* ws = static_cast<const char*>(workspace);
-  dim3 grid(batch * s_q, kHeads / 8, 1);
-  mla_combine_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
-      reinterpret_cast<const int*>(ws + L.reqs), reinterpret_cast<const float*>(ws + L.part_lse),
-      reinterpret_cast<const float*>(ws + L.part_o), s_q, (flags & MLA_FLAG_OUT_FP32) ? 1 : 0, out, lse);
-  return last_cuda_error();
+  // a programmatic dependent of the decode kernel: scheduled while the decode
+  // kernel's last units finish, it waits for that grid before reading
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(batch * s_q, kHeads / 8, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e =
+      cudaLaunchKernelEx(&cfg, mla_combine_kernel, reinterpret_cast<const int*>(ws + L.reqs),
+                         reinterpret_cast<const float*>(ws + L.part_lse), reinterpret_cast<const float*>(ws + L.part_o),
+                         s_q, (flags & MLA_FLAG_OUT_FP32) ? 1 : 0, out, lse);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return MLA_ERR_CUDA;
+  }
+  return MLA_OK;
 }
 
 int mla_workspace_status(const void* workspace, mla_stream_t stream) {

@@ -6,6 +6,7 @@
 
 #include "common.cuh"
 #include "plan.cuh"
+#include "ptx.cuh"
 
 namespace mla {
 
@@ -47,6 +48,7 @@ __global__ void __launch_bounds__(1024) mla_plan_kernel(const int* __restrict__ 
                                                         int* req_meta, int slots_cap) {
   __shared__ int s_warp[32];
   __shared__ int s_prefix[kPlanSmemReqs];
+  grid_launch_dependents();  // the decode kernel may set up now; it waits for this grid before reading the plan
   const bool prefix_in_smem = B <= kPlanSmemReqs;
   int carry = 0, tot = 0;
   for (int base = 0; base < B; base += blockDim.x) {
@@ -102,6 +104,7 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(const int* __restrict_
                                                           const float* __restrict__ part_lse,
                                                           const float* __restrict__ part_o, int s_q,
                                                           int out_fp32, void* out, float* lse) {
+  grid_dependency_wait();  // the decode kernel has finished (programmatic dependent launch)
   const int bt = blockIdx.x;
   const int b = bt / s_q, t = bt - b * s_q;
   const int ns = req_meta[4 * b + 1];

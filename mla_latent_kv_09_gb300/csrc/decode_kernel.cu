@@ -149,6 +149,8 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
   const int unit = cluster_id % U;
   const int tok = cluster_id / U;
   const bool s_side = rank == 0;
+  grid_launch_dependents();  // the combine kernel may be scheduled now; it waits for this grid
+  grid_dependency_wait();    // the plan of this step is complete (programmatic dependent launch)
 
   {  // a unit with no work leaves at once (both CTAs see the same range)
     const int* um = p.unit_meta + 5 * unit;
@@ -730,8 +732,10 @@ cudaError_t decode_set_attrs() {
   return cudaFuncSetAttribute(mla_decode_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
 }
 
+// `dependent`: may be scheduled while the previous kernel on the stream (the
+// plan) finishes (programmatic dependent launch).
 static void cluster_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, int num_clusters,
-                           cudaStream_t stream, bool sparse) {
+                           cudaStream_t stream, bool sparse, bool dependent) {
   cfg = cudaLaunchConfig_t{};
   cfg.gridDim = dim3(2 * num_clusters, 1, 1);
   cfg.blockDim = dim3(decode_threads(sparse), 1, 1);
@@ -741,23 +745,25 @@ static void cluster_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, i
   attr[0].val.clusterDim.x = 2;  // the kernel always runs as CTA pairs
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = dependent ? 2 : 1;
 }
 
 // Co-resident 2-CTA clusters of the decode kernel on the current device.
 cudaError_t decode_max_clusters(int* n, int num_clusters_hint) {
   cudaLaunchConfig_t cfg;
-  cudaLaunchAttribute attr[1];
-  cluster_config(cfg, attr, num_clusters_hint, nullptr, false);
+  cudaLaunchAttribute attr[2];
+  cluster_config(cfg, attr, num_clusters_hint, nullptr, false, false);
   return cudaOccupancyMaxActiveClusters(n, mla_decode_kernel<false>, &cfg);
 }
 
 cudaError_t decode_launch(bool sparse, int num_clusters, cudaStream_t stream, const DecodeParams& p,
                           const CUtensorMap& tm_q, const CUtensorMap& tm_kv) {
   cudaLaunchConfig_t cfg;
-  cudaLaunchAttribute attr[1];
-  cluster_config(cfg, attr, num_clusters, stream, sparse);
+  cudaLaunchAttribute attr[2];
+  cluster_config(cfg, attr, num_clusters, stream, sparse, true);
   return sparse ? cudaLaunchKernelEx(&cfg, mla_decode_kernel<true>, p, tm_q, tm_kv)
                 : cudaLaunchKernelEx(&cfg, mla_decode_kernel<false>, p, tm_q, tm_kv);
 }

@@ -218,11 +218,12 @@ mla_decode_mtp_kernel(const __grid_constant__ DecodeParams p, const __grid_const
   const int lane = threadIdx.x & 31;
   const int unit = blockIdx.x >> 2;
 
-  {  // a unit with no work leaves at once (all four CTAs see the same range)
-    const int* um = p.unit_meta + 5 * unit;
-    if (um[0] >= p.batch || (um[0] == um[2] && um[1] >= um[3])) return;
-  }
+  // The set-up below overlaps the end of the plan kernel (a programmatic
+  // dependency); nothing the plan writes is read before grid_dependency_wait.
+  // The combine kernel may be scheduled at once: it waits for this grid too.
+  grid_launch_dependents();
   if (mis > kAlignSlack) {  // never touch shared memory past the end of the allocation
+    grid_dependency_wait();
     if (threadIdx.x == 0) atomicCAS(p.ws_hdr + kHdrStatus, 0, static_cast<int>(kStWorkspace));
     return;
   }
@@ -284,6 +285,7 @@ mla_decode_mtp_kernel(const __grid_constant__ DecodeParams p, const __grid_const
   cluster_sync();  // every CTA's barriers exist before any remote operation
   tc_fence_after();
   const uint32_t tmem = misc[0];
+  grid_dependency_wait();  // the plan (unit ranges, request table) is complete
 
   Ctl ctl;
   ctl.abort = &misc[1];
@@ -348,16 +350,22 @@ mla_decode_mtp_kernel(const __grid_constant__ DecodeParams p, const __grid_const
         if (g > 0 && !(ok = wait_bar<false>(bar(kHand + ((g - 1u) & 1u)), ((g - 1u) >> 1) & 1u, ctl))) break;
         tc_fence_after();
         const uint32_t dS = tmem + kColS + 128u * sb;
-        // K = 576 in 36 steps of 16, one 64-dim chunk per slot
+        // K = 576 in 36 steps of 16, one 64-dim chunk per slot.  The next slot
+        // group is probed (without blocking) one chunk into the current one:
+        // a blocking wait, even on a completed barrier, stalls this thread for
+        // ~150 cycles, in which the shallow MMA queue runs dry.
+        uint32_t next_ready = 0;
 #pragma unroll
         for (int c = 0; c < kNumChunks; ++c) {
           const uint32_t uc = u + c;
           const uint32_t G = uc / kKGroup;
           if (c == 6) mbar_arrive_relaxed(bar(kHand + sb));  // the other issuer may start its tile
           if (c > 0 && c % kKGroup == 0) {  // the next slot group (the first was waited for above)
-            if (!(ok = wait_bar<true>(kf0 + 8u * (G % kKGroups), (G / kKGroups) & 1u, ctl))) break;
+            if (!next_ready && !(ok = wait_bar<true>(kf0 + 8u * (G % kKGroups), (G / kKGroups) & 1u, ctl))) break;
             tc_fence_after();
           }
+          if (c % kKGroup == 1 && c + kKGroup < kNumChunks + 1)
+            next_ready = mbar_test_wait_cluster(kf0 + 8u * ((G + 1u) % kKGroups), ((G + 1u) / kKGroups) & 1u);
           const uint64_t bd = smem_desc(slot0 + (uc % kKSlots) * kPageChunk, 16u, 1024u);
           if (c < 8) {
 #pragma unroll
@@ -935,8 +943,11 @@ mla_decode_mtp_kernel(const __grid_constant__ DecodeParams p, const __grid_const
   }
 }
 
+// Launch configuration; `dependent`: may start while the previous kernel on
+// the stream (the plan) finishes (programmatic dependent launch).
 template <bool kBf16PV>
-void cluster_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, int num_clusters, cudaStream_t stream) {
+void cluster_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, int num_clusters, cudaStream_t stream,
+                    bool dependent) {
   cfg = cudaLaunchConfig_t{};
   cfg.gridDim = dim3(4 * num_clusters, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
@@ -946,8 +957,10 @@ void cluster_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, int num_
   attr[0].val.clusterDim.x = 4;  // two SM pairs
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = dependent ? 2 : 1;
 }
 
 }  // namespace mtp
@@ -964,8 +977,8 @@ cudaError_t mtp_set_attrs() {
 // Co-resident 4-CTA clusters of the two-token kernel on the current device.
 cudaError_t mtp_max_clusters(int* n, int num_clusters_hint) {
   cudaLaunchConfig_t cfg;
-  cudaLaunchAttribute attr[1];
-  mtp::cluster_config<false>(cfg, attr, num_clusters_hint, nullptr);
+  cudaLaunchAttribute attr[2];
+  mtp::cluster_config<false>(cfg, attr, num_clusters_hint, nullptr, false);
   return cudaOccupancyMaxActiveClusters(n, mtp::mla_decode_mtp_kernel<false>, &cfg);
 }
 
@@ -973,8 +986,8 @@ cudaError_t mtp_launch(bool bf16_pv, int num_clusters, cudaStream_t stream, cons
                        const CUtensorMap& tm_q, const CUtensorMap& tm_k3, const CUtensorMap& tm_v2,
                        const CUtensorMap& tm_out, const CUtensorMap& tm_part) {
   cudaLaunchConfig_t cfg;
-  cudaLaunchAttribute attr[1];
-  mtp::cluster_config<false>(cfg, attr, num_clusters, stream);
+  cudaLaunchAttribute attr[2];
+  mtp::cluster_config<false>(cfg, attr, num_clusters, stream, true);
   return bf16_pv
       ? cudaLaunchKernelEx(&cfg, mtp::mla_decode_mtp_kernel<true>, p, tm_q, tm_k3, tm_v2, tm_out, tm_part)
       : cudaLaunchKernelEx(&cfg, mtp::mla_decode_mtp_kernel<false>, p, tm_q, tm_k3, tm_v2, tm_out, tm_part);

@@ -87,6 +87,31 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
   return ok != 0;
 }
 
+// Non-blocking probe with cluster-scope acquire: 1 if the phase of `parity`
+// has completed.  The result is consumed later, so the probe's latency
+// overlaps the instructions issued in between.
+__device__ __forceinline__ uint32_t mbar_test_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n"
+      " mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+  return ok;
+}
+
+// ---------------------------------------------------------------- dependent launches
+// Wait until the grids this one depends on (launched before it on the stream
+// with programmatic serialization) have completed and their writes are
+// visible; a no-op without such a dependency.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Let the next grid on the stream (if launched as a programmatic dependent)
+// be scheduled now; it still waits for this grid's completion before it
+// reads what this grid writes.
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- cluster
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
