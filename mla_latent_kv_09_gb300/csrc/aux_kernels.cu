@@ -47,9 +47,13 @@ __global__ void __launch_bounds__(1024) mla_plan_kernel(const int* __restrict__ 
                                                         int tile_rows, int U, int* hdr, int* unit_meta,
                                                         int* req_meta, int slots_cap) {
   __shared__ int s_warp[32];
-  __shared__ int s_prefix[kPlanSmemReqs];
+  __shared__ int s_prefix[kPlanSmemReqs];  // exclusive cost prefix per request
+  __shared__ int s_tiles[kPlanSmemReqs];   // tiles per request
   grid_launch_dependents();  // the decode kernel may set up now; it waits for this grid before reading the plan
-  const bool prefix_in_smem = B <= kPlanSmemReqs;
+  // Up to kPlanSmemReqs requests the table is built in shared memory and each
+  // request's row is written once; beyond, the global rows hold the pass-one
+  // values in between.
+  const bool in_smem = B <= kPlanSmemReqs;
   int carry = 0, tot = 0;
   for (int base = 0; base < B; base += blockDim.x) {
     const int b = base + threadIdx.x;
@@ -57,9 +61,13 @@ __global__ void __launch_bounds__(1024) mla_plan_kernel(const int* __restrict__ 
     const int c = plan_cost(n);
     const int incl = block_inclusive_scan(c, s_warp, tot);
     if (b < B) {
-      req_meta[4 * b + 0] = n;
-      req_meta[4 * b + 3] = carry + incl - c;
-      if (prefix_in_smem) s_prefix[b] = carry + incl - c;
+      if (in_smem) {
+        s_prefix[b] = carry + incl - c;
+        s_tiles[b] = n;
+      } else {
+        req_meta[4 * b + 0] = n;
+        req_meta[4 * b + 3] = carry + incl - c;
+      }
     }
     carry += tot;
   }
@@ -69,18 +77,19 @@ __global__ void __launch_bounds__(1024) mla_plan_kernel(const int* __restrict__ 
   carry = 0;
   for (int base = 0; base < B; base += blockDim.x) {
     const int b = base + threadIdx.x;
-    int ns = 0;
-    if (b < B) ns = plan_n_splits(req_meta[4 * b + 3], req_meta[4 * b + 0], W, U);
+    int n = 0, pre = 0, ns = 0;
+    if (b < B) {
+      n = in_smem ? s_tiles[b] : req_meta[4 * b + 0];
+      pre = in_smem ? s_prefix[b] : req_meta[4 * b + 3];
+      ns = plan_n_splits(pre, n, W, U);
+    }
     const int need = ns > 1 ? ns : 0;
     const int incl = block_inclusive_scan(need, s_warp, tot);
-    if (b < B) {
-      req_meta[4 * b + 1] = ns;
-      req_meta[4 * b + 2] = carry + incl - need;
-    }
+    if (b < B) reinterpret_cast<int4*>(req_meta)[b] = make_int4(n, ns, carry + incl - need, pre);
     carry += tot;
   }
   __syncthreads();
-  auto prefix = [&](int b) { return prefix_in_smem ? s_prefix[b] : req_meta[4 * b + 3]; };
+  auto prefix = [&](int b) { return in_smem ? s_prefix[b] : req_meta[4 * b + 3]; };
   for (int u = threadIdx.x; u < U; u += blockDim.x) {
     const UnitInfo ui = plan_unit(u, W, total, B, prefix);
     int* m = unit_meta + 5 * u;

@@ -415,6 +415,8 @@ mla_decode_mtp_kernel(const __grid_constant__ DecodeParams p, const __grid_const
     const uint32_t srow = stg + ul * 64u, sw = (ul >> 1) & 3u;
     const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * (w & 3)) << 16) + kColO + static_cast<uint32_t>(x0);
     const int nbox = f32 ? 8 : 4, bw = f32 ? 16 : 32;
+    // partial results stay in L2 for the combine kernel; final ones need not
+    const uint64_t pol = to_part ? l2_policy_evict_last() : l2_policy_evict_first();
 #pragma unroll 1
     for (int i = 0; i < nbox; ++i) {
       uint32_t v[16];
@@ -443,7 +445,7 @@ mla_decode_mtp_kernel(const __grid_constant__ DecodeParams p, const __grid_const
       fence_proxy_async_smem();  // generic writes, read next by the tensor store
       __syncwarp();
       if (lane == 0) {
-        tma_store_2d(tm, stg, x0 + bw * i, y);
+        tma_store_2d_hint(tm, stg, x0 + bw * i, y, pol);
         bulk_commit();
       }
     }
@@ -821,7 +823,31 @@ mla_decode_mtp_kernel(const __grid_constant__ DecodeParams p, const __grid_const
         }
       }
     } else {
-      // Value ranks: per page, this rank's 256 value dims.
+      // Value ranks: per page, this rank's 256 value dims, the page's last
+      // read in this step (the score rank read it just before): evict first.
+      // At the start the score ranks' TMA units are the bottleneck (each
+      // holds a limited number of bytes in flight while its Q streams in
+      // from HBM): this rank pulls its token's Q and the first two pages of
+      // that token into L2 meanwhile.
+      const uint64_t pol_v = l2_policy_evict_first();
+      if (lane == 0) {
+        SegIter it0(p, unit);
+        Seg s0;
+        if (it0.next(s0)) {
+          const long long qrow = (static_cast<long long>(s0.b) * 2 + tok) * kHeads;
+          for (int h = 0; h < 2; ++h) bulk_prefetch_l2(p.q + (qrow + h * kPage) * kDqk, kPage * kDqk * 2);
+          const int nl = max(p.cache_lens[s0.b], 0);
+          const int np = (nl + kPage - 1) / kPage;
+          const int* row = p.block_table + static_cast<long long>(s0.b) * p.bt_stride;
+          for (int t = s0.t0; t < s0.t1 && t < s0.t0 + 2; ++t) {
+            const int pi = 2 * t + static_cast<int>(tok);
+            if (pi >= np || pi >= p.bt_stride) break;
+            const int pg = row[pi];
+            if (pg >= 0 && pg < p.num_pages)
+              bulk_prefetch_l2(p.kv + static_cast<long long>(pg) * kPage * kDqk, kPage * kDqk * 2);
+          }
+        }
+      }
       Ring<kVSlots> rv;
       while (ok && it.next(sg)) {
         const int L = max(p.cache_lens[sg.b], 0);
@@ -849,8 +875,8 @@ mla_decode_mtp_kernel(const __grid_constant__ DecodeParams p, const __grid_const
                 // chunks 2 tok, 2 tok + 1 and 4 + 2 tok, 5 + 2 tok: two loads of two chunks
 #pragma unroll
                 for (int h = 0; h < 2; ++h)
-                  tma_load_3d(vslot(rv.idx) + 2 * h * kPageChunk, &tm_v2, 0, y, 4 * h + 2 * static_cast<int>(tok),
-                              bar(kVF + rv.idx));
+                  tma_load_3d_hint(vslot(rv.idx) + 2 * h * kPageChunk, &tm_v2, 0, y,
+                                   4 * h + 2 * static_cast<int>(tok), bar(kVF + rv.idx), pol_v);
               }
               ++issued;
             }
