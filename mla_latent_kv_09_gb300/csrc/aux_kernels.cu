@@ -126,30 +126,55 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(const int* __restrict_
   for (int k = 0; k < 16; ++k) acc[k] = 0.f;
   float LSE = -INFINITY;
   if (ns > 1) {
+    // Lane s (< 32) holds split s's LSE: one round trip for the LSEs, shuffles
+    // for max, sum and weights, then the partial rows of two splits per
+    // batch (eight 16-byte loads in flight per lane).
     const int slot0 = req_meta[4 * b + 2];
-    float m = -INFINITY;
-    for (int s = lane; s < ns; s += 32)
-      m = fmaxf(m, part_lse[(static_cast<long long>(slot0 + s) * s_q + t) * kHeads + h]);
+    auto lse_of = [&](int s) { return part_lse[(static_cast<long long>(slot0 + s) * s_q + t) * kHeads + h]; };
+    const float lse_l = lane < ns ? lse_of(lane) : -INFINITY;
+    float m = lse_l;
+    for (int s = lane + 32; s < ns; s += 32) m = fmaxf(m, lse_of(s));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
     if (m != -INFINITY) {
-      float sum = 0.f;
-      for (int s = lane; s < ns; s += 32)
-        sum += expf(part_lse[(static_cast<long long>(slot0 + s) * s_q + t) * kHeads + h] - m);
+      float sum = lane < ns ? expf(lse_l - m) : 0.f;
+      for (int s = lane + 32; s < ns; s += 32) sum += expf(lse_of(s) - m);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
       LSE = m + logf(sum);
-      for (int s = 0; s < ns; ++s) {
-        const long long prow = (static_cast<long long>(slot0 + s) * s_q + t) * kHeads + h;
-        const float w = expf(part_lse[prow] - LSE);
-        if (w == 0.f) continue;
-        const float4* src = reinterpret_cast<const float4*>(part_o + prow * kDv) + lane;
+      const float w_l = lane < ns ? expf(lse_l - LSE) : 0.f;
+      auto row = [&](int s) {
+        return reinterpret_cast<const float4*>(part_o + ((static_cast<long long>(slot0 + s) * s_q + t) * kHeads + h) * kDv) + lane;
+      };
+      auto add = [&](float w, const float4 (&v)[4]) {
+        if (w == 0.f) return;  // an empty split adds nothing
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const float4 v = src[32 * k];
-          acc[4 * k + 0] += w * v.x; acc[4 * k + 1] += w * v.y;
-          acc[4 * k + 2] += w * v.z; acc[4 * k + 3] += w * v.w;
+          acc[4 * k + 0] += w * v[k].x; acc[4 * k + 1] += w * v[k].y;
+          acc[4 * k + 2] += w * v[k].z; acc[4 * k + 3] += w * v[k].w;
         }
+      };
+      const int n32 = ns < 32 ? ns : 32;
+      int s = 0;
+      for (; s + 2 <= n32; s += 2) {
+        const float4* r0 = row(s);
+        const float4* r1 = row(s + 1);
+        float4 v0[4], v1[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          v0[k] = r0[32 * k];
+          v1[k] = r1[32 * k];
+        }
+        add(__shfl_sync(0xffffffffu, w_l, s), v0);
+        add(__shfl_sync(0xffffffffu, w_l, s + 1), v1);
+      }
+      for (; s < ns; ++s) {  // the odd split, and splits past 32
+        const float w = s < 32 ? __shfl_sync(0xffffffffu, w_l, s) : expf(lse_of(s) - LSE);
+        const float4* r0 = row(s);
+        float4 v0[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) v0[k] = r0[32 * k];
+        add(w, v0);
       }
     }
   }
