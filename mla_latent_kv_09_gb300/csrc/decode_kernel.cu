@@ -51,7 +51,6 @@ constexpr int kStageS = kNumChunks * kChunkBytes;  // 9 chunks: all 576 dims
 constexpr int kStageO = 8 * kChunkBytes;           // 8 chunks: the 512 value dims
 constexpr int kPBytes = kHeads * 128;              // 128 rows x 64 fp16
 constexpr int kQChunkBytes = kHeads * 128;         // Q: 128 rows x 64 bf16, 128B-swizzled
-constexpr int kPrefetch = 4;                       // tiles prefetched into L2 ahead of the TMA
 
 // Shared-memory layout (offsets from a 1024-aligned base).  The barrier block
 // sits at the same offset in both CTAs (multicast commits rely on it).
@@ -532,8 +531,8 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
     // ================================================= TMA producer (whole warp; lane 0 issues)
     // S side: per segment three Q slots, then (dense) one slot per tile.  O
     // side (dense): one slot per tile, value dims only.  Page ids are read 32
-    // at a time with one coalesced load; the S side also prefetches the pages
-    // of tiles kPrefetch ahead into L2.
+    // at a time with one coalesced load.  (No L2 prefetch from this SM: it
+    // would share the TMA unit with the loads and delay them.)
     SegIter it(p, unit);
     Seg sg;
     Ring3 rs;
@@ -565,15 +564,10 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
           const int pg = bt_row[jb + lane];
           my_page = (pg >= 0 && pg < p.num_pages) ? pg : -1;
         }
-        if (s_side && lane < kPrefetch && lane < cnt && my_page >= 0)
-          bulk_prefetch_l2(p.kv + static_cast<long long>(my_page) * kPage * kDqk, kPage * kDqk * 2);
         for (int jj = 0; jj < cnt; ++jj, rs.advance()) {
           const int page = __shfl_sync(0xffffffffu, my_page, jj);
-          const int pf = __shfl_sync(0xffffffffu, my_page, min(jj + kPrefetch, 31));
           if (!(ok = warp_wait(bar(kKE + rs.idx), rs.phase ^ 1u, ctl))) break;
           if (lane == 0) {
-            if (s_side && jj + kPrefetch < cnt && pf >= 0)
-              bulk_prefetch_l2(p.kv + static_cast<long long>(pf) * kPage * kDqk, kPage * kDqk * 2);
             // an entry outside the pool reads the TMA fill value (zeros)
             const int y = page >= 0 ? page * kPage : static_cast<int>(p.num_pages) * kPage;
             mbar_arrive_expect_tx(bar(kKF + rs.idx), nchunks * kChunkBytes);
