@@ -12,27 +12,24 @@
 //
 // One work unit = one 4-CTA cluster = two SM pairs.  A tile is 128 cached
 // rows (two pages).
-//   Ranks 0, 1 (score pair).  Rank r holds token r's Q — dims 0..511 in
-//     tensor memory, the 64 RoPE dims in shared memory — and streams page r
-//     of every tile (all 576 dims) through a ring of 8 KiB chunk slots; Q
-//     dims 0..511 come through the same ring (and tcgen05.cp), the RoPE part
-//     into one of two alternating shared buffers.  Rank 0 issues S = Q K^T for both tokens
-//     (M = 256, N = 128, K = 576) into two alternating 128-column score
-//     buffers; token r's rows land in rank r.  Each rank runs the online
-//     softmax of its token (fp32, exp2 domain, lazy rescale: the reference max
-//     moves only when a score beats it by more than 2^8) and sends P plus the
-//     per-row rescale factor to rank 2 + r with st.async.
+//   Ranks 0, 1 (score pair).  Rank r holds token r's Q — dims 0..511 in tensor
+//     memory, the 64 RoPE dims in shared memory — and streams page r of every
+//     tile (all 576 dims) through a ring of 21 chunk slots of 8 KiB, freed
+//     and refilled in groups of three as soon as the score MMAs reading them
+//     finish; Q dims 0..511 come through the same ring (and tcgen05.cp) at the
+//     start of each segment.  Rank 0 issues S = Q K^T for both tokens (M =
+//     256, N = 128, K = 576) into two alternating 128-column score buffers;
+//     token r's rows land in rank r.  Each rank runs the online softmax of
+//     its token (fp32, exp2 domain, lazy rescale: the reference max moves
+//     only when a score beats it by more than 2^8) and sends P plus the
+//     per-row rescale factor to rank 2 + r.
 //   Ranks 2, 3 (value pair).  Rank 2 + r owns token r's O (128 x 512 fp32,
 //     all of its tensor memory).  Rank 2 + r loads the value dims
 //     [128 r, 128 r + 128) and [256 + 128 r, 256 + 128 r + 128) of both pages
-//     (the B columns it holds in the pair) through a ring of page slots,
-//     converts them to fp16 in place, and rank 2 issues O += P V (M = 256,
-//     N = 2 x 256, K = 128).
-// Loads are latency-bound (HBM latency under this load is about 1.5 us), so
-// both rings free and refill at fine grain: chunk slots in groups of three as
-// soon as the score MMAs reading them finish, a page slot as soon as the value
-// MMAs of that page finish.  The MMA thread waits once per slot group: a wait
-// costs about 170 cycles of issue time, which a group's 12 queued MMAs hide.
+//     (the B columns it holds in the pair) through a ring of page slots, and
+//     rank 2 issues O += P V (M = 256, N = 2 x 256, K = 128).  At the end of
+//     a segment all sixteen warps write O (scaled by 1 / z) with tensor
+//     stores, staged in the P slot the last tile used.
 // P and V are bf16 (the kBf16PV variant, the default), or fp16 on request
 // (11 significant bits on the softmax weights instead of 8; values must then
 // stay below 65504 in magnitude, and V is converted in shared memory).
@@ -40,19 +37,19 @@
 // Warps (640 threads).  Score ranks: 0-15 softmax (warp w: head rows
 // 32 (w % 4) .., key columns 32 (w / 4) .. of each tile), 16 and 19 MMA issue
 // on rank 0 (even and odd tiles; 16 also owns tensor memory and moves Q in),
-// 17 TMA producer, 18 P shipper.  Value ranks: 0-3 O rescale and epilogue
-// (thread i = head row i), 4-15 V conversion, 16 MMA issue on rank 2 and
+// 17 TMA producer, 18 P shipper.  Value ranks: 0-3 O rescale (thread i = head
+// row i), 4-15 V conversion (fp16 variant; rows past the cache end are zeroed
+// in both), 0-15 the segment epilogue, 16 MMA issue on rank 2 and
 // tensor-memory owner, 17 TMA producer.
 //
-// Two threads issue the score MMAs, alternating tiles: a single issuing
-// thread leaves the tensor pipe idle while it waits on a barrier (a wait is
-// ~150 cycles even when the barrier is complete, and the MMA queue holds
-// little more than one MMA).  Each issuer waits for its tile's score buffer
-// and first slot group while the other issues, then takes an issue token from
-// the other and issues its 36 MMAs, waiting for the two later slot groups
-// between them (their loads started only as the tile two back freed its
-// groups), and passes the token on after 24 MMAs.  Tiles thus follow each
-// other in the pipe, which keeps the chunk ring's full lookahead.
+// Two threads issue the score MMAs, alternating tiles: one thread issues
+// these paired MMAs at ~73-110 cycles each while the pipe executes one every
+// 64, so the pipe is full only while both issue.  Each issuer waits for its
+// tile's score buffer (freed by every softmax warp right after its own
+// tensor-memory load) and first slot group while the other issues, takes an
+// issue token from the other, issues its 36 MMAs — probing the next slot
+// group without blocking a few MMAs ahead — and passes the token on after
+// 24 MMAs.
 //
 // P travels as one bulk copy per tile: the softmax warps write it into a
 // local copy laid out as the value rank's A operand; the shipper warp sends
