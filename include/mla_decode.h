@@ -214,6 +214,20 @@ int mla_decode_noalloc(const void* q, const void* kv_cache, int64_t num_pages,
                        float softmax_scale, const int32_t* topk_idx, int topk,
                        unsigned flags, void* out, float* lse, mla_stream_t stream);
 
+/*
+ * Diagnostic of the device-side failure path (no counterpart in the method's
+ * description).  Launches one CTA on `stream` that waits, with the bounded
+ * wait every decode kernel uses, on a shared-memory barrier that nothing
+ * completes.  The wait gives up after its limit (about 2 s), records
+ * MLA_ERR_TIMEOUT in the workspace header (the word mla_workspace_status
+ * reads) and the kernel returns: no trap, no fault, the context stays usable.
+ * `workspace` is a decode workspace of at least 256 bytes (device pointer,
+ * 256-byte aligned); only its status word is written.  Returns MLA_OK once
+ * launched (asynchronous), MLA_ERR_INVALID_ARG for a bad workspace, or a
+ * launch error.
+ */
+int mla_selftest_wait_timeout(void* workspace, size_t ws_bytes, mla_stream_t stream);
+
 /* Human-readable name of a status code (static string). */
 const char* mla_status_string(int status);
 

@@ -41,6 +41,7 @@ from ._binding import (  # noqa: F401
     mla_default_num_units,
     mla_status_string,
     mla_workspace_status,
+    mla_selftest_wait_timeout,
 )
 
 NUM_HEADS = 128

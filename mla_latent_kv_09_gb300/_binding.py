@@ -41,6 +41,7 @@ SIGNATURES = {
                             _uint, _c_int, _vp, _c_size, _vp, _vp, _vp]),
     "mla_combine": (_c_int, [_vp, _c_size, _c_int, _c_int, _c_int, _uint, _c_int, _vp, _vp, _vp]),
     "mla_workspace_status": (_c_int, [_vp, _vp]),
+    "mla_selftest_wait_timeout": (_c_int, [_vp, _c_size, _vp]),
     "mla_decode_noalloc": (_c_int, [_vp, _vp, _i64, _vp, _i64, _vp, _c_int, _c_int, _c_int, _f32, _vp, _c_int,
                                     _uint, _vp, _vp, _vp]),
     "mla_status_string": (ctypes.c_char_p, [_c_int]),
@@ -163,3 +164,8 @@ def mla_decode_noalloc(q, kv_cache, num_pages: int, block_table, bt_stride: int,
 
 def mla_workspace_status(workspace, stream=None) -> int:
     return load().mla_workspace_status(_ptr(workspace), _stream(stream))
+
+
+def mla_selftest_wait_timeout(workspace, ws_bytes: int, stream=None) -> None:
+    _check("mla_selftest_wait_timeout",
+           load().mla_selftest_wait_timeout(_ptr(workspace), int(ws_bytes), _stream(stream)))

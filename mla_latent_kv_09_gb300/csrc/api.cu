@@ -16,6 +16,7 @@
 namespace mla {
 __global__ void mla_plan_kernel(const int* lens, int B, int topk, int tile_rows, int U, int* hdr,
                                 int* unit_meta, int* req_meta, int slots_cap);
+__global__ void mla_wait_timeout_kernel(int* status);
 __global__ void mla_combine_kernel(const int* req_meta, const float* part_lse, const float* part_o,
                                    int s_q, int out_fp32, void* out, float* lse);
 __global__ void mla_validate_kernel(const int* lens, const int* bt, long long bt_stride,
@@ -380,6 +381,15 @@ int mla_combine(void* workspace, size_t ws_bytes, int batch, int s_q, int num_he
     return MLA_ERR_CUDA;
   }
   return MLA_OK;
+}
+
+int mla_selftest_wait_timeout(void* workspace, size_t ws_bytes, mla_stream_t stream) {
+  if (!workspace || ws_bytes < 256 || !aligned(workspace, 256)) return MLA_ERR_INVALID_ARG;
+  int* status = static_cast<int*>(workspace) + kHdrStatus;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(status, 0, sizeof(int), s) != cudaSuccess) return MLA_ERR_CUDA;
+  mla_wait_timeout_kernel<<<1, 32, 0, s>>>(status);
+  return last_cuda_error();
 }
 
 int mla_workspace_status(const void* workspace, mla_stream_t stream) {

@@ -6,6 +6,7 @@
 
 #include "common.cuh"
 #include "plan.cuh"
+#include "kernel_common.cuh"
 #include "ptx.cuh"
 
 namespace mla {
@@ -233,4 +234,25 @@ __global__ void mla_validate_kernel(const int* __restrict__ lens, const int* __r
   }
 }
 
+// ------------------------------------------------------------------ failure-path diagnostic
+// One CTA waits, with the decode kernels' bounded wait, on a barrier that
+// nothing completes; the wait records kStTimeout in *status and gives up.
+__global__ void mla_wait_timeout_kernel(int* status) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ uint32_t abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0u;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  Ctl ctl;
+  ctl.abort = &abort_flag;
+  ctl.n_remote = 0;
+  ctl.status = status;
+  if (threadIdx.x == 0) (void)wait_bar<false>(smem_u32(&bar), 0u, ctl);
+  __syncthreads();
+}
+
 }  // namespace mla
+

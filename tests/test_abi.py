@@ -31,7 +31,7 @@ def test_header_declares_the_three_calls_and_helpers():
     names = declared_functions()
     for n in ["mla_decode_plan", "mla_decode", "mla_combine", "mla_decode_workspace_size",
               "mla_status_string", "mla_default_num_units", "mla_decode_plan_host",
-              "mla_workspace_status"]:
+              "mla_workspace_status", "mla_selftest_wait_timeout"]:
         assert n in names
 
 
@@ -80,6 +80,9 @@ def test_null_pointers_and_bad_shapes_are_rejected_before_any_launch(lib):
     assert f(*a) == m.MLA_ERR_INVALID_ARG
     assert lib.mla_combine(None, 0, 1, 1, 128, 0, 1, ok_ptr, ok_ptr, None) == m.MLA_ERR_INVALID_ARG
     assert lib.mla_decode_plan(None, 1, 1, 0, 1, ok_ptr, 1 << 20, None) == m.MLA_ERR_INVALID_ARG
+    assert lib.mla_selftest_wait_timeout(None, 1 << 20, None) == m.MLA_ERR_INVALID_ARG
+    assert lib.mla_selftest_wait_timeout(ok_ptr, 64, None) == m.MLA_ERR_INVALID_ARG  # smaller than the header
+    assert lib.mla_selftest_wait_timeout(ok_ptr + 16, 1 << 20, None) == m.MLA_ERR_INVALID_ARG  # misaligned
 
 
 def test_python_binding_raises_when_library_missing(tmp_path):

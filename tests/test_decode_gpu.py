@@ -289,3 +289,17 @@ def test_validate_reports_bad_table_and_bad_index():
     with pytest.raises(m.MlaError) as e:
         run(ws, topk_idx=idx, validate=True)
     assert e.value.status == m.MLA_ERR_BAD_INDEX
+
+
+# ---------------------------------------------------------------- failure path (bounded waits)
+
+def test_a_wait_that_runs_out_reports_timeout_and_the_context_stays_usable():
+    # one CTA waits on a barrier nothing completes: the bounded wait gives up
+    # (about 2 s), records MLA_ERR_TIMEOUT and the kernel returns; no fault
+    ws = m.Workspace(1, 1, 0, torch.device("cuda:0"))
+    m.mla_selftest_wait_timeout(ws.buf, ws.nbytes)
+    assert m.mla_workspace_status(ws.buf) == m.MLA_ERR_TIMEOUT
+    assert torch.cuda.is_available() and torch.zeros(4, device="cuda").sum().item() == 0.0
+    w = wl.make_workload("after-timeout", [300, 41], s_q=2, causal=True, seed=5, device="cuda")
+    o, lse = run(w)
+    assert_close(o, lse, *reference(w))
