@@ -21,6 +21,7 @@ import json
 import os
 import statistics
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -79,7 +80,9 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.proc = None
         self.gpu = gpu_index
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+        # raw samples go to $MLA_BENCH_LOG_DIR (default: the temporary directory)
+        log_dir = os.environ.get("MLA_BENCH_LOG_DIR") or tempfile.gettempdir()
+        self.path = os.path.join(log_dir, f"clocks_bench_{os.getpid()}.csv")
 
     def start(self):
         try:
