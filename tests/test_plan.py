@@ -128,3 +128,50 @@ def test_balance_on_uniform_batch_is_tight():
     # makespan: no unit holds more than W = ceil(total cost / U) tiles
     assert max(sizes) <= -(-(32 * (64 + C0)) // 74)
     assert sum(1 for x in sizes if x) >= 72
+
+
+# ---------------------------------------------------------------- device plan vs host mirror
+
+def _align256(x):
+    return (x + 255) // 256 * 256
+
+
+def ws_offsets(B, s_q, U):
+    """Byte offsets of the workspace's unit table and request table, and its
+    size: header (64 ints), unit table (U x 5 ints), request table (B x 4
+    ints), partial LSE and partial O (2U slots), each 256-byte aligned."""
+    off_units = _align256(64 * 4)
+    off_reqs = off_units + _align256(U * 5 * 4)
+    slots = 2 * U
+    total = (off_reqs + _align256(B * 4 * 4) + _align256(slots * s_q * 128 * 4)
+             + _align256(slots * s_q * 128 * 512 * 4))
+    return off_units, off_reqs, total
+
+
+@pytest.mark.parametrize("B,s_q,U", [(1, 1, 1), (64, 2, 36), (200, 1, 74), (37, 2, 5)])
+def test_workspace_offsets_match_the_library(B, s_q, U):
+    assert ws_offsets(B, s_q, U)[2] == m.mla_decode_workspace_size(B, s_q, 128, U)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("seed", range(4))
+def test_device_plan_matches_host_plan_bit_exactly(seed):
+    import torch
+    rng = np.random.default_rng(500 + seed)
+    for s_q, topk in [(1, 0), (2, 0), (2, 512), (1, 2048)]:
+        B = int(rng.integers(1, 200))
+        U = int(rng.integers(1, 80))
+        lens = rng.integers(0, 9000, B).astype(np.int32)
+        lens[rng.random(B) < 0.1] = 0
+        um_h, rm_h = m.mla_decode_plan_host(lens, s_q, topk, U)
+        ws = m.Workspace(B, s_q, U, torch.device("cuda:0"))
+        ws.buf.fill_(0xAB)  # stale bytes must all be overwritten
+        m.mla_decode_plan(torch.from_numpy(lens).cuda(), B, s_q, topk, U, ws.buf, ws.nbytes)
+        torch.cuda.synchronize()
+        assert m.mla_workspace_status(ws.buf) == 0
+        raw = ws.buf.cpu().numpy()
+        off_u, off_r, _ = ws_offsets(B, s_q, U)
+        um_d = raw[off_u:off_u + U * 20].view(np.int32).reshape(U, 5)
+        rm_d = raw[off_r:off_r + B * 16].view(np.int32).reshape(B, 4)
+        assert np.array_equal(um_d, um_h), (s_q, topk, B, U)
+        assert np.array_equal(rm_d, rm_h), (s_q, topk, B, U)
