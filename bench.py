@@ -7,6 +7,12 @@ the pages quote (b = 64 per microbatch).  Inputs are synthetic and resident
 in HBM; the pool exceeds L2 and L2 is also flushed (256 MB write) before
 every timed step.
 
+Before the headline workload the same step is timed on the four other
+decode workloads (one request of 256 tokens; B=32 at 4096 tokens; B=128 at
+32768 tokens with 5% of rows x8; B=80 top-2048 of 65536), each with its
+roofline figures and a bounded oracle sample on the host cores, reported
+under `other_workloads`.
+
 Prints ONE JSON line.  `value` is the whole-job attention throughput in
 TFLOP/s (algorithmic FLOPs of every rank's steps / max-over-ranks time);
 microseconds per call, HBM GB/s and the roofline fractions ride along.
@@ -214,35 +220,27 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
-def run_ours(args, world, rank, local):
+def kernel_name(w) -> str:
+    return "mla_decode_mtp_kernel" if (w.s_q == 2 and not w.topk) else "mla_decode_kernel"
+
+
+def time_step(m, w, args, dev, world, sampler=None):
+    """Times plan + decode + combine on one resident workload.
+
+    Host-launched steps with an event between kernels give the per-kernel
+    split; the timed figure is a CUDA graph of the three calls, replayed
+    (checked bit-identical to the host-launched output).  256 MB of L2 are
+    flushed before every step, outside the events."""
     import torch
 
-    import mla_latent_kv_09_gb300 as m
-    import workloads as wl
-    from mla_latent_kv_09_gb300 import accounting as acc
-    from mla_latent_kv_09_gb300 import build as mbuild
-
-    mbuild.build()
-    m.load()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    w = wl.make_config(args.config, seed=args.seed + rank, device=dev)
     B, s_q = w.batch, w.s_q
-    host_lens = w.cache_lens.cpu().numpy()
-    host_topk = None if w.topk_idx is None else w.topk_idx.cpu().numpy()
-    flops = acc.step_flops(host_lens, s_q, w.causal, host_topk)
-    nbytes = acc.step_bytes(host_lens, s_q, w.causal, host_topk)
-    pk, pk_kind = peaks()
-    ridge = pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)
-    bound = "tensor" if flops / nbytes > ridge else "hbm"
-
     ws = m.Workspace(B, s_q, args.num_units, dev)
     out = torch.empty((B, s_q, 128, 512), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((B, s_q, 128), dtype=torch.float32, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     topk = w.topk
-    flags = (m.MLA_FLAG_CAUSAL if w.causal else 0) | (m.MLA_FLAG_F16_PV if args.f16_pv else 0)
+    flags = (m.MLA_FLAG_CAUSAL if w.causal else 0) | (m.MLA_FLAG_BF16_PV if args.bf16_pv else 0)
     U = ws.num_units
 
     # every call goes to the stream current at call time (the capture stream
@@ -264,15 +262,11 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     status = m.mla_workspace_status(ws.buf, stream.cuda_stream)
     if status != 0:
-        raise RuntimeError(f"device status after warm-up: {m.mla_status_string(status)}")
+        raise RuntimeError(f"{w.name}: device status after warm-up: {m.mla_status_string(status)}")
 
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
-    sampler = ClockSampler(local)
-    sampler.start()
-    time.sleep(0.3)
     barrier(world)
     torch.cuda.synchronize()
-    t_wall = time.perf_counter()
     for i in range(args.steps):
         flush.zero_()
         e = ev[i]
@@ -284,18 +278,17 @@ def run_ours(args, world, rank, local):
         combine()
         e[3].record(stream)
     torch.cuda.synchronize()
-    barrier(world)
-    wall = time.perf_counter() - t_wall
-    launch_ms = sum(e[0].elapsed_time(e[3]) for e in ev) / args.steps
-    dec_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / args.steps
-    plan_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps
-    comb_ms = sum(e[2].elapsed_time(e[3]) for e in ev) / args.steps
-    step_ms = launch_ms
+    r = {"launch_ms": sum(e[0].elapsed_time(e[3]) for e in ev) / args.steps,
+         "dec_ms": sum(e[1].elapsed_time(e[2]) for e in ev) / args.steps,
+         "plan_ms": sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps,
+         "comb_ms": sum(e[2].elapsed_time(e[3]) for e in ev) / args.steps,
+         "num_units": U, "flags": flags}
+    r["step_ms"] = r["launch_ms"]
+    t_wall = time.perf_counter()
     if not args.no_graph:
         # the step as a serving loop runs it: plan + decode + combine recorded
         # once in a CUDA graph (the decode and combine kernels are programmatic
-        # dependents of the kernel before them) and replayed; the loop above,
-        # with an event between kernels, gives the per-kernel split
+        # dependents of the kernel before them) and replayed
         ref_out, ref_lse = out.clone(), lse.clone()
         graph = torch.cuda.CUDAGraph()
         side = torch.cuda.Stream(dev)
@@ -311,6 +304,9 @@ def run_ours(args, world, rank, local):
             graph.replay()
         torch.cuda.synchronize()
         evg = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+        if sampler is not None:
+            sampler.start()
+            time.sleep(0.3)
         barrier(world)
         torch.cuda.synchronize()
         t_wall = time.perf_counter()
@@ -321,16 +317,90 @@ def run_ours(args, world, rank, local):
             evg[i][1].record(stream)
         torch.cuda.synchronize()
         barrier(world)
-        wall = time.perf_counter() - t_wall
-        step_ms = sum(e[0].elapsed_time(e[1]) for e in evg) / args.steps
+        r["step_ms"] = sum(e[0].elapsed_time(e[1]) for e in evg) / args.steps
         status = m.mla_workspace_status(ws.buf, stream.cuda_stream)
         if status != 0:
-            raise RuntimeError(f"device status after the graph replays: {m.mla_status_string(status)}")
+            raise RuntimeError(f"{w.name}: device status after the graph replays: {m.mla_status_string(status)}")
         if not (torch.equal(out, ref_out) and torch.equal(lse, ref_lse)):
-            raise RuntimeError("graph replays changed the output of the step")
+            raise RuntimeError(f"{w.name}: graph replays changed the output of the step")
+    r["wall_s"] = time.perf_counter() - t_wall
+    r["ws"], r["out"], r["lse"] = ws, out, lse
+    return r
+
+
+def roofline_of(w, r, pk, pk_kind, step_ms):
+    """Algorithmic work of the workload and its roofline figures: `roofline`
+    for the attention kernel alone (its event time), `frac_roofline` for the
+    whole call (plan + attention + combine)."""
+    from mla_latent_kv_09_gb300 import accounting as acc
+    host_lens = w.cache_lens.cpu().numpy()
+    host_topk = None if w.topk_idx is None else w.topk_idx.cpu().numpy()
+    flops = acc.step_flops(host_lens, w.s_q, w.causal, host_topk)
+    nbytes = acc.step_bytes(host_lens, w.s_q, w.causal, host_topk)
+    ridge = pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)
+    bound = "tensor" if flops / nbytes > ridge else "hbm"
+    dec_s = r["dec_ms"] * 1e-3
+    if bound == "tensor":
+        achieved, peak, unit = flops / dec_s / 1e12, pk["bf16_tflops"], "TFLOP/s"
+    else:
+        achieved, peak, unit = nbytes / dec_s / 1e9, pk["hbm_gbs"], "GB/s"
+    step_s = step_ms * 1e-3
+    return {
+        "flops": flops, "nbytes": nbytes, "bound": bound,
+        "tflops": flops / step_s / 1e12, "hbm_gbs": nbytes / step_s / 1e9,
+        "frac_tensor_peak": flops / step_s / 1e12 / pk["bf16_tflops"],
+        "frac_hbm_peak": nbytes / step_s / 1e9 / pk["hbm_gbs"],
+        "frac_roofline": max(flops / (pk["bf16_tflops"] * 1e12), nbytes / (pk["hbm_gbs"] * 1e9)) / step_s,
+        "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+                     "frac": achieved / peak, "traffic": measured_traffic(w.name), "kernel": kernel_name(w),
+                     "scope": "attention kernel alone (its CUDA-event time); frac_roofline covers the whole call",
+                     "peak_source": f"{pk_kind} (burst)"},
+    }
+
+
+def run_ours(args, world, rank, local):
+    import torch
+
+    import mla_latent_kv_09_gb300 as m
+    import workloads as wl
+    from mla_latent_kv_09_gb300 import build as mbuild
+
+    mbuild.build()
+    m.load()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pk, pk_kind = peaks()
+
+    # the other workloads first (one at a time, freed after), the headline last
+    others = {}
+    extra = [c for c in (args.also or "").split(",") if c and c != args.config]
+    for name in extra:
+        w = wl.make_config(name, seed=args.seed + rank, device=dev)
+        r = time_step(m, w, args, dev, world)
+        step_ms = max_over_ranks(r["step_ms"], world)
+        rf = roofline_of(w, r, pk, pk_kind, step_ms)
+        entry = {"batch": w.batch, "s_q": w.s_q, "causal": w.causal, "topk": w.topk, "num_units": r["num_units"],
+                 "us_per_call": step_ms * 1e3, "us_per_call_host_launches": r["launch_ms"] * 1e3,
+                 "us_decode_kernel": r["dec_ms"] * 1e3, "us_plan": r["plan_ms"] * 1e3,
+                 "us_combine": r["comb_ms"] * 1e3, "algorithmic_gflop": rf["flops"] / 1e9,
+                 "algorithmic_mb": rf["nbytes"] / 1e6, "tflops": rf["tflops"], "hbm_gbs": rf["hbm_gbs"],
+                 "frac_roofline": rf["frac_roofline"], "roofline": rf["roofline"]}
+        if rank == 0 and world == 1 and not args.no_cpu_baseline:
+            entry["cpu_baseline"] = cpu_baseline(w, wl.host_arrays(w), args.cpu_budget_other)
+        others[name] = entry
+        del w, r
+        torch.cuda.empty_cache()
+
+    w = wl.make_config(args.config, seed=args.seed + rank, device=dev)
+    B, s_q = w.batch, w.s_q
+    sampler = ClockSampler(local)
+    r = time_step(m, w, args, dev, world, sampler=sampler)
     clocks = sampler.stop()
-    step_ms_max = max_over_ranks(step_ms, world)
+    step_ms_max = max_over_ranks(r["step_ms"], world)
+    rf = roofline_of(w, r, pk, pk_kind, step_ms_max)
+    flops = rf["flops"]
     value = world * flops / (step_ms_max * 1e-3) / 1e12
+    ws, out, lse = r["ws"], r["out"], r["lse"]
 
     # end to end through the host-buffer API: inputs copied in, O/LSE copied out, every step
     e2e = None
@@ -349,7 +419,7 @@ def run_ours(args, world, rank, local):
         def e2e_step():
             m.decode_step_host(pin["q"], pin["kv_cache"], pin["block_table"], pin["cache_lens"],
                                w.softmax_scale, device=dev, causal=w.causal, topk_idx=pin.get("topk_idx"),
-                               f16_pv=args.f16_pv, workspace=ws, dev_buffers=dbuf, out_host=o_h,
+                               bf16_pv=args.bf16_pv, workspace=ws, dev_buffers=dbuf, out_host=o_h,
                                lse_host=l_h)
 
         for _ in range(3):
@@ -366,45 +436,35 @@ def run_ours(args, world, rank, local):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        host = wl.host_arrays(w)
-        cpu = cpu_baseline(w, host, args.cpu_budget)
+        cpu = cpu_baseline(w, wl.host_arrays(w), args.cpu_budget)
 
     if rank != 0:
         return
-    dec_s = dec_ms * 1e-3
-    if bound == "tensor":
-        achieved, peak, unit = flops / dec_s / 1e12, pk["bf16_tflops"], "TFLOP/s"
-    else:
-        achieved, peak, unit = nbytes / dec_s / 1e9, pk["hbm_gbs"], "GB/s"
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_ms_max, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": args.config, "batch": B, "s_q": s_q, "heads": 128, "d_qk": 576, "d_v": 512,
-                   "page": 64, "causal": w.causal, "topk": topk, "num_units": U,
+                   "page": 64, "causal": w.causal, "topk": w.topk, "num_units": r["num_units"],
+                   "value_product": "bf16 P and V" if args.bf16_pv else "fp16 P and V",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "256 MB L2 flush before every timed step; cache pool exceeds L2",
-                   "algorithmic_gflop": flops / 1e9, "algorithmic_mb": nbytes / 1e6},
+                   "algorithmic_gflop": flops / 1e9, "algorithmic_mb": rf["nbytes"] / 1e6},
         "us_per_call": step_ms_max * 1e3,
         "launch": "CUDA graph of plan + decode + combine, replayed" if not args.no_graph
                   else "plan, decode, combine launched from the host",
-        "us_per_call_host_launches": launch_ms * 1e3,
-        "us_decode_kernel": dec_ms * 1e3, "us_plan": plan_ms * 1e3, "us_combine": comb_ms * 1e3,
-        "tflops": flops / (step_ms * 1e-3) / 1e12,
-        "hbm_gbs": nbytes / (step_ms * 1e-3) / 1e9,
-        "frac_tensor_peak": flops / (step_ms * 1e-3) / 1e12 / pk["bf16_tflops"],
-        "frac_hbm_peak": nbytes / (step_ms * 1e-3) / 1e9 / pk["hbm_gbs"],
-        "frac_roofline": max(flops / (pk["bf16_tflops"] * 1e12), nbytes / (pk["hbm_gbs"] * 1e9))
-                         / (step_ms * 1e-3),
-        "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
-                     "frac": achieved / peak, "traffic": measured_traffic(args.config),
-                     "kernel": "mla_decode_mtp_kernel" if (s_q == 2 and not topk) else "mla_decode_kernel",
-                     "peak_source": f"{pk_kind} (burst)"},
+        "us_per_call_host_launches": r["launch_ms"] * 1e3,
+        "us_decode_kernel": r["dec_ms"] * 1e3, "us_plan": r["plan_ms"] * 1e3, "us_combine": r["comb_ms"] * 1e3,
+        "tflops": rf["tflops"], "hbm_gbs": rf["hbm_gbs"],
+        "frac_tensor_peak": rf["frac_tensor_peak"], "frac_hbm_peak": rf["frac_hbm_peak"],
+        "frac_roofline": rf["frac_roofline"],
+        "roofline": rf["roofline"],
         "gpu_launches": 3 * args.steps,
         "clocks": clocks,
         "e2e": e2e,
         "cpu_baseline": cpu,
-        "wall_s_timed_region": wall,
+        "wall_s_timed_region": r["wall_s"],
+        "other_workloads": others,
     }
     print(json.dumps(line), flush=True)
 
@@ -422,10 +482,15 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true",
                     help="time the step from host launches instead of a CUDA graph replay")
-    ap.add_argument("--f16-pv", action="store_true",
-                    help="two-token dense path: value product with fp16 P and V (MLA_FLAG_F16_PV)")
+    ap.add_argument("--bf16-pv", action="store_true",
+                    help="two-token dense path: value product with bf16 P and V (MLA_FLAG_BF16_PV)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--cpu-budget", type=float, default=15.0,
+                    help="seconds of oracle work for the headline workload's CPU baseline")
+    ap.add_argument("--cpu-budget-other", type=float, default=4.0,
+                    help="seconds of oracle work for each other workload's CPU baseline")
+    ap.add_argument("--also", default="single,uniform_b32,long_b128,sparse_b80",
+                    help="other workloads timed before the headline one (comma-separated; '' for none)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -37,8 +37,13 @@
  *  - Every pointer is a DEVICE pointer unless stated otherwise.  The caller
  *    owns all memory; the library allocates nothing.
  *  - The return value reports errors detectable on the host (bad arguments,
- *    unsupported shapes or device, launch failures).  No call synchronises
- *    the stream, except mla_decode with MLA_FLAG_VALIDATE.
+ *    unsupported shapes or device, launch failures).  Errors found on the
+ *    device (validate mode, a wait that ran out) are recorded in the
+ *    workspace's status word; the kernels of the step that find it set leave
+ *    their outputs unwritten, and mla_workspace_status (mla_noalloc_status
+ *    for the built-in workspace) reports it.  Only those two status queries
+ *    synchronise the stream; every other call is asynchronous and can be
+ *    recorded into a CUDA graph.
  *  - Fixed shapes: 128 query heads, 576 q/k dims, 512 value dims, 64-token
  *    pages.  Anything else returns MLA_ERR_UNSUPPORTED.  The device must be
  *    compute capability 10.3 (GB300); there is no other code path.
@@ -68,19 +73,25 @@ typedef enum {
   MLA_ERR_DEVICE = 5,       /* no sm_103 device current                     */
   MLA_ERR_BAD_TABLE = 6,    /* validate mode: block-table entry / length out of range */
   MLA_ERR_BAD_INDEX = 7,    /* validate mode: top-k index outside [-1, len) */
-  MLA_ERR_TIMEOUT = 8       /* a device-side wait ran out (kernel bailed out) */
+  MLA_ERR_TIMEOUT = 8,      /* a device-side wait ran out (kernel bailed out) */
+  MLA_ERR_VALUE_RANGE = 9   /* validate mode: a value dim the step reads is not
+                               finite or does not fit fp16 (|v| >= 65536) */
 } mla_status;
 
 enum {
   MLA_FLAG_CAUSAL = 1,   /* s_q = 2 MTP decode: token t sees [0, len - s_q + t] */
   MLA_FLAG_OUT_FP32 = 2, /* O is written as fp32 instead of bf16           */
-  MLA_FLAG_VALIDATE = 4, /* check table / lengths / indices first (syncs)   */
-  MLA_FLAG_F16_PV = 8    /* s_q = 2 dense only: the value product takes the
-                            softmax weights and values in fp16 (11 significant
-                            bits on the weights) instead of bf16 (8 bits);
-                            V must then stay below 65504 in magnitude and is
-                            converted in shared memory (slower); the s_q = 1
-                            and top-k paths always use fp16               */
+  MLA_FLAG_VALIDATE = 4, /* check lengths, table, indices and value range
+                            first; see mla_decode                           */
+  MLA_FLAG_BF16_PV = 8   /* s_q = 2 dense only: the value product takes the
+                            softmax weights and values in bf16 (8 significant
+                            bits on the weights) instead of the default fp16
+                            (11 bits).  No value-range limit, but on a peaked
+                            softmax (a few rows of large magnitude dominating)
+                            the O error grows to a few times 2e-2.  Every
+                            other path, and this one by default, computes the
+                            value product in fp16: value dims must then stay
+                            below 65504 in magnitude                        */
 };
 
 enum { MLA_NUM_HEADS = 128, MLA_D_QK = 576, MLA_D_V = 512, MLA_PAGE = 64 };
@@ -160,9 +171,15 @@ int mla_decode_plan_host(const int32_t* cache_lens_host, int batch, int s_q,
  *                is visible (O is then 0)
  * Out-of-range table entries or indices never fault: dense page loads
  * outside the pool read zeros, sparse rows outside it are skipped; results
- * for such requests are meaningless.  MLA_FLAG_VALIDATE detects them
- * first: it runs a check kernel, synchronises the stream and returns
- * MLA_ERR_BAD_TABLE / MLA_ERR_BAD_INDEX without launching the attention.
+ * for such requests are meaningless.  MLA_FLAG_VALIDATE detects them first:
+ * a check kernel runs before the attention on the same stream and records
+ * MLA_ERR_BAD_TABLE, MLA_ERR_BAD_INDEX or (wherever the value product is
+ * fp16, i.e. everywhere but the MLA_FLAG_BF16_PV two-token path)
+ * MLA_ERR_VALUE_RANGE for a visible value dim that is not finite or has
+ * |v| >= 65536; the attention and combine kernels then leave O and LSE
+ * unwritten.  It reads every visible cache row once more (a full pass over
+ * the cache: a debugging aid, not a production mode).  The call does not
+ * synchronise: read the outcome with mla_workspace_status.
  * A device-side wait that runs out (about 2 s) makes the kernel record
  * MLA_ERR_TIMEOUT in the workspace and return; mla_workspace_status reads it.
  */
@@ -184,8 +201,9 @@ int mla_combine(void* workspace, size_t ws_bytes, int batch, int s_q,
 
 /*
  * Synchronise `stream` and return the device-side status recorded in the
- * workspace (MLA_OK, MLA_ERR_TIMEOUT, or a plan overflow as
- * MLA_ERR_WORKSPACE).
+ * workspace: MLA_OK; MLA_ERR_BAD_TABLE, MLA_ERR_BAD_INDEX or
+ * MLA_ERR_VALUE_RANGE from validate mode; MLA_ERR_TIMEOUT; or a plan
+ * overflow as MLA_ERR_WORKSPACE.  mla_decode_plan resets it to MLA_OK.
  */
 int mla_workspace_status(const void* workspace, mla_stream_t stream);
 
@@ -206,13 +224,30 @@ int mla_workspace_status(const void* workspace, mla_stream_t stream);
  * the array's device address (with that device current); make that first
  * call before any stream capture.  All calls share the array: calls whose
  * work overlaps on the GPU (other streams, other host threads) race and must
- * be serialised by the caller.
+ * be serialised by the caller.  Errors found on the device (validate mode, a
+ * wait that ran out) are read with mla_noalloc_status.
  */
 int mla_decode_noalloc(const void* q, const void* kv_cache, int64_t num_pages,
                        const int32_t* block_table, int64_t bt_stride,
                        const int32_t* cache_lens, int batch, int s_q, int num_heads,
                        float softmax_scale, const int32_t* topk_idx, int topk,
                        unsigned flags, void* out, float* lse, mla_stream_t stream);
+
+/*
+ * Synchronise `stream` and return the status word of the built-in workspace
+ * of mla_decode_noalloc on the current device: the codes of
+ * mla_workspace_status (a failed validation, a wait that ran out).  Each
+ * mla_decode_noalloc call resets it when its plan runs.
+ */
+int mla_noalloc_status(mla_stream_t stream);
+
+/*
+ * Device address and size in bytes of the built-in workspace on the current
+ * device (looked up on first use, like mla_decode_noalloc), for diagnostics
+ * such as mla_selftest_wait_timeout.  Returns MLA_ERR_INVALID_ARG for null
+ * pointers.
+ */
+int mla_noalloc_workspace(void** dev_ptr, size_t* bytes);
 
 /*
  * Diagnostic of the device-side failure path (no counterpart in the method's

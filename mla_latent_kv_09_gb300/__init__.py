@@ -23,9 +23,10 @@ from ._binding import (  # noqa: F401
     MLA_ERR_INVALID_ARG,
     MLA_ERR_TIMEOUT,
     MLA_ERR_UNSUPPORTED,
+    MLA_ERR_VALUE_RANGE,
     MLA_ERR_WORKSPACE,
     MLA_FLAG_CAUSAL,
-    MLA_FLAG_F16_PV,
+    MLA_FLAG_BF16_PV,
     MLA_FLAG_OUT_FP32,
     MLA_FLAG_VALIDATE,
     MLA_OK,
@@ -35,6 +36,8 @@ from ._binding import (  # noqa: F401
     mla_combine,
     mla_decode,
     mla_decode_noalloc,
+    mla_noalloc_status,
+    mla_noalloc_workspace,
     mla_decode_plan,
     mla_decode_plan_host,
     mla_decode_workspace_size,
@@ -62,13 +65,16 @@ class Workspace:
 
 
 def decode_step(q, kv_cache, block_table, cache_lens, softmax_scale: float, *, causal: bool = False,
-                topk_idx=None, out_fp32: bool = False, validate: bool = False, f16_pv: bool = False,
+                topk_idx=None, out_fp32: bool = False, validate: bool = False, bf16_pv: bool = False,
                 num_units: int = 0, workspace: Workspace | None = None, out=None, lse=None, stream=None):
     """One MLA decode step on device tensors: plan, attention, combine.
 
     q [B, s_q, 128, 576] bf16; kv_cache [num_pages, 64, 576] bf16;
     block_table [B, W] int32; cache_lens [B] int32; topk_idx [B, s_q, k]
-    int32 or None.  f16_pv selects MLA_FLAG_F16_PV (two-token dense path).
+    int32 or None.  bf16_pv selects MLA_FLAG_BF16_PV (two-token dense path:
+    faster, less precise value product).  With validate=True the inputs are
+    checked on the device first and the step's status is read back (a host
+    synchronisation) and raised as MlaError if it is not MLA_OK.
     Returns (O [B, s_q, 128, 512] bf16 or fp32, LSE fp32).
     """
     import torch
@@ -85,17 +91,23 @@ def decode_step(q, kv_cache, block_table, cache_lens, softmax_scale: float, *, c
         stream = torch.cuda.current_stream(q.device)
     topk = 0 if topk_idx is None else topk_idx.shape[-1]
     flags = (MLA_FLAG_CAUSAL if causal else 0) | (MLA_FLAG_OUT_FP32 if out_fp32 else 0) | (
-        MLA_FLAG_VALIDATE if validate else 0) | (MLA_FLAG_F16_PV if f16_pv else 0)
+        MLA_FLAG_VALIDATE if validate else 0) | (MLA_FLAG_BF16_PV if bf16_pv else 0)
     mla_decode_plan(cache_lens, B, s_q, topk, U, workspace.buf, workspace.nbytes, stream)
     mla_decode(q, kv_cache, kv_cache.shape[0], block_table, block_table.stride(0), cache_lens, B, s_q,
                NUM_HEADS, softmax_scale, topk_idx, topk, flags, U, workspace.buf, workspace.nbytes, out,
                lse, stream)
     mla_combine(workspace.buf, workspace.nbytes, B, s_q, NUM_HEADS, flags, U, out, lse, stream)
+    if validate:
+        # the check runs on the device; its outcome is read back here (the
+        # C calls themselves never synchronise for it)
+        status = mla_workspace_status(workspace.buf, stream)
+        if status != MLA_OK:
+            raise MlaError("mla_decode (validate)", status)
     return out, lse
 
 
 def decode_step_host(q, kv_cache, block_table, cache_lens, softmax_scale: float, *, device="cuda",
-                     causal: bool = False, topk_idx=None, out_fp32: bool = False, f16_pv: bool = False,
+                     causal: bool = False, topk_idx=None, out_fp32: bool = False, bf16_pv: bool = False,
                      num_units: int = 0,
                      workspace: Workspace | None = None, dev_buffers=None, out_host=None, lse_host=None):
     """decode_step for HOST tensors (pinned for speed): H2D copies, the step,
@@ -115,7 +127,7 @@ def decode_step_host(q, kv_cache, block_table, cache_lens, softmax_scale: float,
 
     o, l = decode_step(up("q", q), up("kv_cache", kv_cache), up("block_table", block_table),
                        up("cache_lens", cache_lens), softmax_scale, causal=causal,
-                       topk_idx=up("topk_idx", topk_idx), out_fp32=out_fp32, f16_pv=f16_pv,
+                       topk_idx=up("topk_idx", topk_idx), out_fp32=out_fp32, bf16_pv=bf16_pv,
                        num_units=num_units,
                        workspace=workspace, out=d.get("out"), lse=d.get("lse"))
     if out_host is None:

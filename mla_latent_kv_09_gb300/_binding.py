@@ -23,11 +23,12 @@ MLA_ERR_DEVICE = 5
 MLA_ERR_BAD_TABLE = 6
 MLA_ERR_BAD_INDEX = 7
 MLA_ERR_TIMEOUT = 8
+MLA_ERR_VALUE_RANGE = 9
 
 MLA_FLAG_CAUSAL = 1
 MLA_FLAG_OUT_FP32 = 2
 MLA_FLAG_VALIDATE = 4
-MLA_FLAG_F16_PV = 8
+MLA_FLAG_BF16_PV = 8
 
 # every symbol include/mla_decode.h declares: name -> (restype, argtypes)
 _c_int, _c_size, _vp, _i64, _f32, _uint = (ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p,
@@ -44,6 +45,8 @@ SIGNATURES = {
     "mla_selftest_wait_timeout": (_c_int, [_vp, _c_size, _vp]),
     "mla_decode_noalloc": (_c_int, [_vp, _vp, _i64, _vp, _i64, _vp, _c_int, _c_int, _c_int, _f32, _vp, _c_int,
                                     _uint, _vp, _vp, _vp]),
+    "mla_noalloc_status": (_c_int, [_vp]),
+    "mla_noalloc_workspace": (_c_int, [ctypes.POINTER(_vp), ctypes.POINTER(_c_size)]),
     "mla_status_string": (ctypes.c_char_p, [_c_int]),
 }
 
@@ -169,3 +172,15 @@ def mla_workspace_status(workspace, stream=None) -> int:
 def mla_selftest_wait_timeout(workspace, ws_bytes: int, stream=None) -> None:
     _check("mla_selftest_wait_timeout",
            load().mla_selftest_wait_timeout(_ptr(workspace), int(ws_bytes), _stream(stream)))
+
+
+def mla_noalloc_status(stream=None) -> int:
+    """Status word of mla_decode_noalloc's built-in workspace (synchronises the stream)."""
+    return load().mla_noalloc_status(_stream(stream))
+
+
+def mla_noalloc_workspace():
+    """(device address, bytes) of mla_decode_noalloc's built-in workspace on the current device."""
+    ptr, n = ctypes.c_void_p(), ctypes.c_size_t()
+    _check("mla_noalloc_workspace", load().mla_noalloc_workspace(ctypes.byref(ptr), ctypes.byref(n)))
+    return ptr.value, n.value

@@ -17,11 +17,11 @@ namespace mla {
 __global__ void mla_plan_kernel(const int* lens, int B, int topk, int tile_rows, int U, int* hdr,
                                 int* unit_meta, int* req_meta, int slots_cap);
 __global__ void mla_wait_timeout_kernel(int* status);
-__global__ void mla_combine_kernel(const int* req_meta, const float* part_lse, const float* part_o,
-                                   int s_q, int out_fp32, void* out, float* lse);
+__global__ void mla_combine_kernel(const int* hdr, const int* req_meta, const float* part_lse,
+                                   const float* part_o, int s_q, int out_fp32, void* out, float* lse);
 __global__ void mla_validate_kernel(const int* lens, const int* bt, long long bt_stride,
                                     long long num_pages, int B, int s_q, const int* topk_idx, int topk,
-                                    int* status);
+                                    const uint16_t* kv, int check_range, int* status);
 int decode_smem_bytes();
 int decode_threads(bool sparse);
 cudaError_t decode_set_attrs();
@@ -251,43 +251,59 @@ int mla_decode_plan_host(const int32_t* lens, int batch, int s_q, int topk, int 
   return slots <= 2 * num_units ? MLA_OK : MLA_ERR_WORKSPACE;
 }
 
-int mla_decode(const void* q, const void* kv_cache, int64_t num_pages, const int32_t* block_table,
-               int64_t bt_stride, const int32_t* cache_lens, int batch, int s_q, int num_heads,
-               float softmax_scale, const int32_t* topk_idx, int topk, unsigned flags, int num_units,
-               void* workspace, size_t ws_bytes, void* out, float* lse, mla_stream_t stream) {
-  if (!q || !kv_cache || !block_table || !cache_lens || !workspace || !out || !lse) return MLA_ERR_INVALID_ARG;
+}  // extern "C"
+
+// Host-side checks of mla_decode's arguments (shared with the allocation-free
+// step, which runs them before it touches its workspace).
+int mla::check_decode_args(const void* q, const void* kv_cache, int64_t num_pages, const int32_t* block_table,
+                          int64_t bt_stride, const int32_t* cache_lens, int batch, int s_q, int num_heads,
+                          float softmax_scale, const int32_t* topk_idx, int topk, unsigned flags, const void* out,
+                          const float* lse) {
+  if (!q || !kv_cache || !block_table || !cache_lens || !out || !lse) return MLA_ERR_INVALID_ARG;
   if (batch < 1 || num_pages < 1 || bt_stride < 1 || topk < 0) return MLA_ERR_INVALID_ARG;
   if ((topk_idx == nullptr) != (topk == 0)) return MLA_ERR_INVALID_ARG;
-  if (flags & ~static_cast<unsigned>(MLA_FLAG_CAUSAL | MLA_FLAG_OUT_FP32 | MLA_FLAG_VALIDATE | MLA_FLAG_F16_PV))
+  if (flags & ~static_cast<unsigned>(MLA_FLAG_CAUSAL | MLA_FLAG_OUT_FP32 | MLA_FLAG_VALIDATE | MLA_FLAG_BF16_PV))
     return MLA_ERR_INVALID_ARG;
   if (num_heads != kHeads || s_q < 1 || s_q > 2) return MLA_ERR_UNSUPPORTED;
   if (!std::isfinite(softmax_scale) || !(softmax_scale > 0.f)) return MLA_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(out, 16) || !aligned(lse, 4) ||
-      !aligned(block_table, 4) || !aligned(cache_lens, 4) || !aligned(workspace, 256) ||
-      (topk_idx && !aligned(topk_idx, 4)))
+      !aligned(block_table, 4) || !aligned(cache_lens, 4) || (topk_idx && !aligned(topk_idx, 4)))
     return MLA_ERR_INVALID_ARG;
   if (num_pages > (INT32_MAX / kPage) - 1) return MLA_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(batch) * s_q * kHeads > INT32_MAX) return MLA_ERR_UNSUPPORTED;
-  DeviceState* st = nullptr;
-  int rc = device_state(&st);
+  return MLA_OK;
+}
+
+extern "C" {
+
+int mla_decode(const void* q, const void* kv_cache, int64_t num_pages, const int32_t* block_table,
+               int64_t bt_stride, const int32_t* cache_lens, int batch, int s_q, int num_heads,
+               float softmax_scale, const int32_t* topk_idx, int topk, unsigned flags, int num_units,
+               void* workspace, size_t ws_bytes, void* out, float* lse, mla_stream_t stream) {
+  int rc = check_decode_args(q, kv_cache, num_pages, block_table, bt_stride, cache_lens, batch, s_q, num_heads,
+                                 softmax_scale, topk_idx, topk, flags, out, lse);
   if (rc != MLA_OK) return rc;
+  if (!workspace || !aligned(workspace, 256)) return MLA_ERR_INVALID_ARG;
+  DeviceState* st = nullptr;
+  if ((rc = device_state(&st)) != MLA_OK) return rc;
   int U = 0;
   if ((rc = resolve_units(s_q, num_units, &U)) != MLA_OK) return rc;
   const WsLayout L = ws_layout(batch, s_q, U);
   if (ws_bytes < L.total) return MLA_ERR_WORKSPACE;
   char* ws = static_cast<char*>(workspace);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool pair_path = plan_tile_rows(s_q, topk) == 128;
 
   if (flags & MLA_FLAG_VALIDATE) {
+    // the check records the first problem in the workspace status word; the
+    // attention and combine kernels then leave their outputs unwritten, and
+    // mla_workspace_status reports the code (no host synchronisation here)
     int* status = reinterpret_cast<int*>(ws + L.hdr) + kHdrStatus;
-    mla_validate_kernel<<<batch < 1024 ? batch : 1024, 128, 0, s>>>(cache_lens, block_table, bt_stride,
-                                                                    num_pages, batch, s_q, topk_idx, topk, status);
+    const int check_range = (pair_path && (flags & MLA_FLAG_BF16_PV)) ? 0 : 1;  // fp16 value product
+    mla_validate_kernel<<<batch < 1024 ? batch : 1024, 256, 0, s>>>(
+        cache_lens, block_table, bt_stride, num_pages, batch, s_q, topk_idx, topk,
+        static_cast<const uint16_t*>(kv_cache), check_range, status);
     if ((rc = last_cuda_error()) != MLA_OK) return rc;
-    int h = 0;
-    if (cudaMemcpyAsync(&h, status, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
-        cudaStreamSynchronize(s) != cudaSuccess)
-      return MLA_ERR_CUDA;
-    if (h != 0) return h;
   }
 
   DecodeParams p;
@@ -315,7 +331,6 @@ int mla_decode(const void* q, const void* kv_cache, int64_t num_pages, const int
   p.part_o = reinterpret_cast<float*>(ws + L.part_o);
 
   // the two-token kernel moves Q through its 8 KiB chunk slots: 64-row boxes
-  const bool pair_path = plan_tile_rows(s_q, topk) == 128;
   CUtensorMap tm_q, tm_kv;
   if ((rc = encode_2d(&tm_q, q, static_cast<uint64_t>(batch) * s_q * kHeads, pair_path ? kPage : kHeads)) !=
       MLA_OK)
@@ -335,7 +350,7 @@ int mla_decode(const void* q, const void* kv_cache, int64_t num_pages, const int
       return rc;
     if ((rc = encode_out_2d(&tm_part, p.part_o, static_cast<uint64_t>(L.slots) * s_q * kHeads, true)) != MLA_OK)
       return rc;
-    e = mtp_launch((flags & MLA_FLAG_F16_PV) == 0, U, s, p, tm_q, tm_k3, tm_v2, tm_out, tm_part);
+    e = mtp_launch((flags & MLA_FLAG_BF16_PV) != 0, U, s, p, tm_q, tm_k3, tm_v2, tm_out, tm_part);
   } else {
     e = decode_launch(topk_idx != nullptr, U * s_q, s, p, tm_q, tm_kv);
   }
@@ -349,7 +364,7 @@ int mla_decode(const void* q, const void* kv_cache, int64_t num_pages, const int
 int mla_combine(void* workspace, size_t ws_bytes, int batch, int s_q, int num_heads, unsigned flags,
                 int num_units, void* out, float* lse, mla_stream_t stream) {
   if (!workspace || !out || !lse || batch < 1) return MLA_ERR_INVALID_ARG;
-  if (flags & ~static_cast<unsigned>(MLA_FLAG_CAUSAL | MLA_FLAG_OUT_FP32 | MLA_FLAG_VALIDATE | MLA_FLAG_F16_PV))
+  if (flags & ~static_cast<unsigned>(MLA_FLAG_CAUSAL | MLA_FLAG_OUT_FP32 | MLA_FLAG_VALIDATE | MLA_FLAG_BF16_PV))
     return MLA_ERR_INVALID_ARG;
   if (num_heads != kHeads || s_q < 1 || s_q > 2) return MLA_ERR_UNSUPPORTED;
   if (!aligned(out, 16) || !aligned(lse, 4) || !aligned(workspace, 256)) return MLA_ERR_INVALID_ARG;
@@ -373,7 +388,8 @@ int mla_combine(void* workspace, size_t ws_bytes, int batch, int s_q, int num_he
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   const cudaError_t e =
-      cudaLaunchKernelEx(&cfg, mla_combine_kernel, reinterpret_cast<const int*>(ws + L.reqs),
+      cudaLaunchKernelEx(&cfg, mla_combine_kernel, reinterpret_cast<const int*>(ws + L.hdr),
+                         reinterpret_cast<const int*>(ws + L.reqs),
                          reinterpret_cast<const float*>(ws + L.part_lse), reinterpret_cast<const float*>(ws + L.part_o),
                          s_q, (flags & MLA_FLAG_OUT_FP32) ? 1 : 0, out, lse);
   if (e != cudaSuccess) {
@@ -414,6 +430,7 @@ const char* mla_status_string(int status) {
     case MLA_ERR_BAD_TABLE: return "MLA_ERR_BAD_TABLE: cache length or block-table entry out of range";
     case MLA_ERR_BAD_INDEX: return "MLA_ERR_BAD_INDEX: top-k index outside [-1, cache length)";
     case MLA_ERR_TIMEOUT: return "MLA_ERR_TIMEOUT: a device-side wait ran out";
+    case MLA_ERR_VALUE_RANGE: return "MLA_ERR_VALUE_RANGE: a visible value dim is not finite or too large for fp16";
     default: return "unknown mla_status";
   }
 }

@@ -110,11 +110,13 @@ __global__ void __launch_bounds__(1024) mla_plan_kernel(const int* __restrict__ 
 // Grid (B * s_q, 128 / 8); warp w of a block merges head blockIdx.y * 8 + w.
 // Requests with one split were finished by the decode kernel; requests with
 // no tiles get O = 0, LSE = -inf.
-__global__ void __launch_bounds__(256) mla_combine_kernel(const int* __restrict__ req_meta,
+__global__ void __launch_bounds__(256) mla_combine_kernel(const int* __restrict__ hdr,
+                                                          const int* __restrict__ req_meta,
                                                           const float* __restrict__ part_lse,
                                                           const float* __restrict__ part_o, int s_q,
                                                           int out_fp32, void* out, float* lse) {
   grid_dependency_wait();  // the decode kernel has finished (programmatic dependent launch)
+  if (hdr[kHdrStatus] != 0) return;  // a failed check or wait: the step's outputs stay unwritten
   const int bt = blockIdx.x;
   const int b = bt / s_q, t = bt - b * s_q;
   const int ns = req_meta[4 * b + 1];
@@ -200,23 +202,60 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(const int* __restrict_
 
 // ------------------------------------------------------------------ validate
 // Checks lengths, the block-table entries the step will read and the top-k
-// indices; records the first problem found in the status word.
+// indices, and (check_range) that every value dim the step reads is finite
+// and converts to fp16 without overflow, i.e. |v| < 65536 as a bf16 pattern
+// below 0x4780; records the first problem found in the status word.  One
+// CTA per request (grid-strided); reading the value dims of every visible row
+// makes this a full pass over the visible cache.
 __global__ void mla_validate_kernel(const int* __restrict__ lens, const int* __restrict__ bt,
                                     long long bt_stride, long long num_pages, int B, int s_q,
-                                    const int* __restrict__ topk_idx, int topk, int* status) {
+                                    const int* __restrict__ topk_idx, int topk, const uint16_t* __restrict__ kv,
+                                    int check_range, int* status) {
+  __shared__ int s_bad;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+  // value dims 0..511 of pool row `row`: one warp, 16 B per lane, 2 rounds
+  auto row_in_range = [&](long long row) {
+    const uint4* src = reinterpret_cast<const uint4*>(kv + row * kDqk);
+    bool ok = true;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const uint4 v = __ldg(src + lane + 32 * k);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        ok = ok && (w[i] & 0x7fffu) < 0x4780u && ((w[i] >> 16) & 0x7fffu) < 0x4780u;
+    }
+    return __all_sync(0xffffffffu, ok);
+  };
   for (int b = blockIdx.x; b < B; b += gridDim.x) {
+    if (threadIdx.x == 0) s_bad = 0;
+    __syncthreads();
     const int L = lens[b];
     const int* row = bt + static_cast<long long>(b) * bt_stride;
-    if (L < 0) { atomicCAS(status, 0, static_cast<int>(kStBadTable)); continue; }
-    if (topk_idx == nullptr) {
+    if (L < 0) {
+      if (threadIdx.x == 0) atomicCAS(status, 0, static_cast<int>(kStBadTable));
+    } else if (topk_idx == nullptr) {
       if (static_cast<long long>(L) > bt_stride * kPage) {
-        atomicCAS(status, 0, static_cast<int>(kStBadTable));
-        continue;
-      }
-      const int np = (L + kPage - 1) / kPage;
-      for (int j = threadIdx.x; j < np; j += blockDim.x) {
-        const int pg = row[j];
-        if (pg < 0 || pg >= num_pages) atomicCAS(status, 0, static_cast<int>(kStBadTable));
+        if (threadIdx.x == 0) atomicCAS(status, 0, static_cast<int>(kStBadTable));
+      } else {
+        const int np = (L + kPage - 1) / kPage;
+        for (int j = threadIdx.x; j < np; j += blockDim.x) {
+          const int pg = row[j];
+          if (pg < 0 || pg >= num_pages) {
+            atomicCAS(status, 0, static_cast<int>(kStBadTable));
+            s_bad = 1;
+          }
+        }
+        __syncthreads();
+        if (check_range && !s_bad) {
+          for (int j = warp; j < L; j += nwarps) {
+            const long long r = static_cast<long long>(row[j / kPage]) * kPage + j % kPage;
+            if (!row_in_range(r)) {
+              if (lane == 0) atomicCAS(status, 0, static_cast<int>(kStValueRange));
+              break;
+            }
+          }
+        }
       }
     } else {
       const int* ix = topk_idx + static_cast<long long>(b) * s_q * topk;
@@ -224,13 +263,29 @@ __global__ void mla_validate_kernel(const int* __restrict__ lens, const int* __r
         const int v = ix[k];
         if (v < -1 || v >= L) {
           atomicCAS(status, 0, static_cast<int>(kStBadIndex));
+          s_bad = 1;
         } else if (v >= 0) {
           const long long pi = v / kPage;
-          if (pi >= bt_stride || row[pi] < 0 || row[pi] >= num_pages)
+          if (pi >= bt_stride || row[pi] < 0 || row[pi] >= num_pages) {
             atomicCAS(status, 0, static_cast<int>(kStBadTable));
+            s_bad = 1;
+          }
+        }
+      }
+      __syncthreads();
+      if (check_range && !s_bad) {
+        for (int k = warp; k < s_q * topk; k += nwarps) {
+          const int v = ix[k];
+          if (v < 0) continue;
+          const long long r = static_cast<long long>(row[v / kPage]) * kPage + v % kPage;
+          if (!row_in_range(r)) {
+            if (lane == 0) atomicCAS(status, 0, static_cast<int>(kStValueRange));
+            break;
+          }
         }
       }
     }
+    __syncthreads();  // s_bad is reset for the next request
   }
 }
 

@@ -42,7 +42,13 @@ __host__ __device__ inline WsLayout ws_layout(int batch, int s_q, int num_units)
 enum { kHdrStatus = 0, kHdrUnits = 1, kHdrWidth = 2, kHdrTotal = 3, kHdrSlots = 4 };
 
 // Device status codes (same numbering as the public mla_status).
-enum { kStOk = 0, kStWorkspace = 3, kStBadTable = 6, kStBadIndex = 7, kStTimeout = 8 };
+enum { kStOk = 0, kStWorkspace = 3, kStBadTable = 6, kStBadIndex = 7, kStTimeout = 8, kStValueRange = 9 };
+
+// Host-side argument checks of mla_decode (status code; MLA_OK = 0).
+int check_decode_args(const void* q, const void* kv_cache, int64_t num_pages, const int32_t* block_table,
+                      int64_t bt_stride, const int32_t* cache_lens, int batch, int s_q, int num_heads,
+                      float softmax_scale, const int32_t* topk_idx, int topk, unsigned flags, const void* out,
+                      const float* lse);
 
 struct DecodeParams {
   const uint16_t* q;          // bf16 [B, s_q, 128, 576]

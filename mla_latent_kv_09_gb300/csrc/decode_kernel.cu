@@ -151,9 +151,13 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
   grid_launch_dependents();  // the combine kernel may be scheduled now; it waits for this grid
   grid_dependency_wait();    // the plan of this step is complete (programmatic dependent launch)
 
-  {  // a unit with no work leaves at once (both CTAs see the same range)
+  {  // a unit with no work leaves at once (both CTAs see the same range), and
+     // so does every unit once the step's status word is set (a failed
+     // validation): the plan and the check are complete here, and nothing
+     // else writes the word before this grid's own waits could run out
     const int* um = p.unit_meta + 5 * unit;
     if (um[0] >= p.batch || (um[0] == um[2] && um[1] >= um[3])) return;
+    if (p.ws_hdr[kHdrStatus] != 0) return;
   }
   if (mis > kAlignSlack) {  // never touch shared memory past the end of the allocation
     if (threadIdx.x == 0) atomicCAS(p.ws_hdr + kHdrStatus, 0, static_cast<int>(kStWorkspace));

@@ -75,6 +75,8 @@ constexpr int kKGroup = 3;                        // chunk slots per landing / f
 constexpr int kKGroups = kKSlots / kKGroup;
 constexpr int kVPage = 4 * kPageChunk;            // 32 KiB: one page, this rank's 256 value dims
 constexpr int kVSlots = 4;                        // value ranks: page slots (two tiles)
+constexpr int kVDepth = 1;                        // fp16 variant: pages of value loads in flight per thread
+                                                  // beyond the one being stored (2 measured no faster)
 // P tile, 128 heads x 128 keys of 16-bit weights, as a K-major 128B-swizzled
 // operand whose 8-row groups hold both 64-key halves side by side: byte
 // (row / 8) * 2048 + half * 1024 + (row % 8) * 128 + swizzled 16-B piece.  A
@@ -88,11 +90,11 @@ constexpr int kQChunk = kHeads * 128;             // 16 KiB: 128 heads x 64 dims
 // the same offset in all four CTAs, which multicast commits rely on).
 constexpr int kOffStage = 0;                         // chunk slots (score ranks) / page slots (value ranks)
 constexpr int kOffQr = kKSlots * kPageChunk;         // score ranks: Q dims 512..575
-constexpr int kOffXchg = kOffQr + kQChunk;           // score ranks: row max / sum exchange, 6 KiB
-constexpr int kOffPs = kOffXchg + 6144;              // score ranks: outgoing P tile (same layout as kOffP)
+constexpr int kOffXchg = kOffQr + kQChunk;           // score ranks: row max / sums exchange, 8 KiB
+constexpr int kOffPs = kOffXchg + 8192;              // score ranks: outgoing P tile (same layout as kOffP)
 constexpr int kOffAlphaS = kOffPs + kPSlot;          // score ranks: outgoing float[128] rescale factors
 constexpr int kOffFinS = kOffAlphaS + kHeads * 4;    // score ranks: outgoing float[128] final scales
-constexpr int kEndS = kOffFinS + kHeads * 4;         // 228352
+constexpr int kEndS = kOffFinS + kHeads * 4;         // 230400
 constexpr int kOffP = kVSlots * kVPage;              // value ranks: [2] P tiles
 constexpr int kOffAlpha = kOffP + 2 * kPSlot;        // value ranks: float[2][128]
 constexpr int kOffFin = kOffAlpha + 2 * kHeads * 4;  // value ranks: float[2][128]
@@ -283,6 +285,11 @@ mla_decode_mtp_kernel(const __grid_constant__ DecodeParams p, const __grid_const
   tc_fence_after();
   const uint32_t tmem = misc[0];
   grid_dependency_wait();  // the plan (unit ranges, request table) is complete
+  // a set status word (a failed validation) leaves this step's outputs
+  // unwritten: every role skips its work and the CTAs go straight to the
+  // teardown (the plan and the check are complete here, and nothing else
+  // writes the word before this grid's own waits could run out)
+  const bool halt = p.ws_hdr[kHdrStatus] != 0;
 
   Ctl ctl;
   ctl.abort = &misc[1];
@@ -450,7 +457,9 @@ mla_decode_mtp_kernel(const __grid_constant__ DecodeParams p, const __grid_const
     __syncwarp();
   };
 
-  if (score_rank && warp < kSoftmaxWarps) {
+  if (halt) {
+    // nothing to do
+  } else if (score_rank && warp < kSoftmaxWarps) {
     // ================================================= softmax (score ranks)
     // Warp (q4, cg): head rows 32 q4 .. +31 (its tensor-memory lane quarter),
     // key columns 32 cg .. +31 of the tile.  The four warps of a quarter
@@ -467,7 +476,7 @@ mla_decode_mtp_kernel(const __grid_constant__ DecodeParams p, const __grid_const
     float* fin_out = reinterpret_cast<float*>(smem + kOffFinS);
     const uint32_t rSE = mapa(bar(kSE), 0);
     float* xmax = reinterpret_cast<float*>(smem + kOffXchg);                   // [2 parity][4 cg][128]
-    float* xsum = reinterpret_cast<float*>(smem + kOffXchg + 8 * kHeads * 4);  // [4 cg][128]
+    float* xsum = reinterpret_cast<float*>(smem + kOffXchg + 8 * kHeads * 4);  // [2 sum][4 cg][128]
     const int qbar = 1 + q4;
     SegIter it(p, unit);
     Seg sg;
@@ -477,10 +486,11 @@ mla_decode_mtp_kernel(const __grid_constant__ DecodeParams p, const __grid_const
       const int L = max(p.cache_lens[sg.b], 0);
       const int vis = p.causal ? L - 1 + static_cast<int>(tok) : L;
       const long long bt_row = static_cast<long long>(sg.b) * 2 + tok;
-      // z: sum of the fp32 weights; it normalises O and gives the LSE (O then
-      // carries the weights' 16-bit rounding once more, relative <= 2^-11 for
-      // fp16 and 2^-9 for bf16)
-      float m_used = NEG_INF, z = 0.f;
+      // zr: sum of the 16-bit weights the value product uses; it normalises O,
+      // so O is a convex combination of value rows and a weight's rounding
+      // error acts on (v_j - O) instead of v_j.  zx: sum of the fp32 weights,
+      // for the LSE.  Each warp keeps the sums of its own 32 key columns.
+      float m_used = NEG_INF, zr = 0.f, zx = 0.f;
       for (int j = sg.t0; j < sg.t1; ++j, ++g) {
         const uint32_t sb = g & 1u, ph = (g >> 1) & 1u;
         const bool last = (j == sg.t1 - 1);
@@ -525,23 +535,34 @@ mla_decode_mtp_kernel(const __grid_constant__ DecodeParams p, const __grid_const
         if (mt > m_used + kRescaleLog2) {
           alpha = (m_used == NEG_INF) ? 0.f : ex2_approx(m_used - mt);
           m_used = mt;
-          z *= alpha;
+          zr *= alpha;
+          zx *= alpha;
         }
         uint32_t pk[16];
         if (m_used == NEG_INF) {
 #pragma unroll
           for (int c = 0; c < 16; ++c) pk[c] = 0u;
         } else {
-          float ze[4] = {0.f, 0.f, 0.f, 0.f};
+          // the 16-bit weights are summed exactly: a bf16 pattern is the top
+          // half of the fp32 pattern of the same value; an fp16 pattern moved
+          // up by 13 bits is the fp32 pattern of the same value times 2^-112
+          // (normal and subnormal alike), the 2^112 is applied once per tile
+          float zs[4] = {0.f, 0.f, 0.f, 0.f}, ze[4] = {0.f, 0.f, 0.f, 0.f};
           const float nm = -m_used;
 #pragma unroll
           for (int c = 0; c < 16; ++c) {
             const float p0 = ex2_approx(fmaf(s[2 * c], p.scale_log2, nm));
             const float p1 = ex2_approx(fmaf(s[2 * c + 1], p.scale_log2, nm));
             pk[c] = kBf16PV ? pack_bf16x2(p0, p1) : pack_f16x2(p0, p1);
+            if (kBf16PV)
+              zs[c & 3] += __uint_as_float(pk[c] << 16) + __uint_as_float(pk[c] & 0xffff0000u);
+            else
+              zs[c & 3] += __uint_as_float((pk[c] << 13) & 0x0fffe000u) +
+                           __uint_as_float((pk[c] >> 3) & 0x0fffe000u);
             ze[c & 3] += p0 + p1;
           }
-          z += (ze[0] + ze[1]) + (ze[2] + ze[3]);
+          zr += ((zs[0] + zs[1]) + (zs[2] + zs[3])) * (kBf16PV ? 1.f : 5.192296858534828e33f);  // 2^112
+          zx += (ze[0] + ze[1]) + (ze[2] + ze[3]);
         }
         // ---- the local P copy: free once the previous tile's bulk copy read it
         if (g > 0) ok = ok && warp_wait(bar(kPsFree), (g - 1u) & 1u, ctl);
@@ -553,15 +574,17 @@ mla_decode_mtp_kernel(const __grid_constant__ DecodeParams p, const __grid_const
           if (lead) alpha_out[row] = alpha;
         }
         if (last) {  // ---- segment end: the quarter's partial sums -> final scale and LSE
-          xsum[cg * kHeads + row] = z;
+          xsum[cg * kHeads + row] = zr;
+          xsum[(4 + cg) * kHeads + row] = zx;
           if (!named_bar_all(qbar, 128, ok)) {
             stop = true;
             break;
           }
           if (lead) {
-            const float zt = (z + xsum[kHeads + row]) + (xsum[2 * kHeads + row] + xsum[3 * kHeads + row]);
-            fin_out[row] = zt > 0.f ? 1.f / zt : 0.f;  // O_final = O_acc / z
-            const float lse = zt > 0.f ? (m_used + log2f(zt)) * 0.69314718055994531f : NEG_INF;
+            const float zrt = (zr + xsum[kHeads + row]) + (xsum[2 * kHeads + row] + xsum[3 * kHeads + row]);
+            const float zxt = (zx + xsum[5 * kHeads + row]) + (xsum[6 * kHeads + row] + xsum[7 * kHeads + row]);
+            fin_out[row] = zrt > 0.f ? 1.f / zrt : 0.f;  // O_final = O_acc / zr
+            const float lse = zxt > 0.f ? (m_used + log2f(zxt)) * 0.69314718055994531f : NEG_INF;
             if (sg.slot < 0) {
               p.lse[bt_row * kHeads + row] = lse;
             } else if (sg.slot < 2 * U) {  // the plan never uses more than 2 * (U - 1) slots
@@ -846,7 +869,28 @@ mla_decode_mtp_kernel(const __grid_constant__ DecodeParams p, const __grid_const
         }
       }
       Ring<kVSlots> rv;
-      while (ok && it.next(sg)) {
+      if (!kBf16PV) {
+        // fp16 variant: the conversion warps load the value dims themselves;
+        // this warp announces each stored page to rank 2 (a release at
+        // cluster scope, cumulative over the group's writes it observed at
+        // named barrier 8) and votes with the group at barrier 7
+        const uint32_t rVR = mapa(bar(kVR), 2);
+        bool go = true;
+        while (go && it.next(sg)) {
+          for (int j = sg.t0; j < sg.t1 && go; ++j) {
+            for (int e = 0; e < 2; ++e, rv.advance()) {
+              const bool w_ok = warp_wait(bar(kVE + rv.idx), rv.phase ^ 1u, ctl);
+              if (!named_bar_all(7, kConvThreads + 32, w_ok)) {
+                go = false;
+                break;
+              }
+              named_bar_sync(8, kConvThreads + 32);
+              if (lane == 0) mbar_arrive_remote(rVR + 8u * rv.idx);
+            }
+          }
+        }
+      }
+      while (kBf16PV && ok && it.next(sg)) {
         const int L = max(p.cache_lens[sg.b], 0);
         const int* bt_row = p.block_table + static_cast<long long>(sg.b) * p.bt_stride;
         const int npages = (L + kPage - 1) / kPage;
@@ -887,8 +931,106 @@ mla_decode_mtp_kernel(const __grid_constant__ DecodeParams p, const __grid_const
         }
       }
     }
+  } else if (!score_rank && warp < kMmaWarp && !kBf16PV) {
+    // ================================================= V loads + fp16 conversion (value ranks, warps 4-15)
+    // fp16 variant.  Each page of this rank's value dims (64 rows x the
+    // 128-dim halves [128 tok, +128) and [256 + 128 tok, +128)) is read from
+    // global memory into registers (an L2 hit: the score rank has just
+    // loaded the page), converted to fp16 and stored in the slot's 128B-
+    // swizzled layout, the one the tensor loads give the bf16 variant.  Warp
+    // w (0-11) owns rows w, w + 12, .. of a page; lanes 0-15 the first half
+    // of a row, lanes 16-31 the second, 16 B each.  Staging through registers
+    // instead of converting a landed tile in place halves this SM's shared-
+    // memory traffic for V and frees a slot as soon as its value product is
+    // done: the next page is loaded while the warps wait for the next free
+    // slot.  Rows past the cache end (and pages outside the pool) are stored
+    // as zeros, so whatever lies there cannot reach O.
+    const int ptid = threadIdx.x - 128;
+    const int lw = ptid >> 5;
+    const int hs = lane >> 4, kp = lane & 15;
+    const int gcol = 64 * (4 * hs + 2 * static_cast<int>(tok) + (kp >> 3)) + 8 * (kp & 7);
+    const uint32_t scol = static_cast<uint32_t>((2 * hs + (kp >> 3)) * kPageChunk);
+    const uint32_t spc = static_cast<uint32_t>(kp & 7);
+    constexpr int kRowsPerThread = (kPage + 11) / 12;  // 6: rows lw + 12 i
+    const volatile float* fin_s = reinterpret_cast<const volatile float*>(smem + kOffFin);
+    // kVDepth pages of loads in flight per thread (registers), so that a
+    // page's load latency spans several pages' turns
+    uint4 v[kVDepth][kRowsPerThread];
+    // page pi of the current segment's request (pool page, or -1 past the
+    // cache end / outside the pool) into buffer d; rows >= L - 64 pi are zeros
+    auto load_page = [&](uint4 (&dst)[kRowsPerThread], const int* bt_row, int L, int pi) {
+      int page = -1;
+      if (pi < (L + kPage - 1) / kPage && pi < p.bt_stride) {
+        const int pg = __ldg(bt_row + pi);
+        page = (pg >= 0 && pg < p.num_pages) ? pg : -1;
+      }
+      const int rows = L - pi * kPage;
+      const uint16_t* src = p.kv + static_cast<long long>(page >= 0 ? page : 0) * (kPage * kDqk) + gcol;
+#pragma unroll
+      for (int i = 0; i < kRowsPerThread; ++i) {
+        const int r = lw + 12 * i;
+        dst[i] = (page >= 0 && r < kPage && r < rows) ? ld_global_nc_v4(src + r * kDqk) : make_uint4(0u, 0u, 0u, 0u);
+      }
+    };
+    SegIter it(p, unit);
+    Seg sg;
+    Ring<kVSlots> rv;
+    uint32_t g = 0, nseg = 0;
+    bool stop = false;  // the twelve warps vote at every named barrier
+    while (!stop && it.next(sg)) {
+      const int L = max(p.cache_lens[sg.b], 0);
+      const int* bt_row = p.block_table + static_cast<long long>(sg.b) * p.bt_stride;
+      const int p0 = 2 * sg.t0, np = 2 * (sg.t1 - sg.t0);  // this segment's pages: p0 .. p0 + np - 1
+#pragma unroll
+      for (int d = 0; d < kVDepth; ++d)
+        if (d < np) load_page(v[d], bt_row, L, p0 + d);
+      for (int q0 = 0; q0 < np && !stop; q0 += kVDepth) {
+#pragma unroll
+        for (int d = 0; d < kVDepth; ++d) {
+          const int q = q0 + d;
+          if (q >= np) break;
+          const bool ok = warp_wait(bar(kVE + rv.idx), rv.phase ^ 1u, ctl);  // PV is done with the slot
+          if (!named_bar_all(7, kConvThreads + 32, ok)) {  // with the announcing warp
+            stop = true;
+            break;
+          }
+          const uint32_t stg = vslot(rv.idx) + scol;
+#pragma unroll
+          for (int i = 0; i < kRowsPerThread; ++i) {
+            const int r = lw + 12 * i;
+            if (r < kPage)
+              st_shared_v4(stg + static_cast<uint32_t>(r) * 128u + ((spc ^ static_cast<uint32_t>(r & 7)) << 4),
+                           bf16x2_to_f16x2(v[d][i].x), bf16x2_to_f16x2(v[d][i].y), bf16x2_to_f16x2(v[d][i].z),
+                           bf16x2_to_f16x2(v[d][i].w));
+          }
+          fence_proxy_async_smem();  // generic writes, read next by the tensor core
+          // the TMA warp, which has no loads in flight, announces the page: a
+          // release arrive from a thread of this group would first wait for
+          // its own prefetch loads of the next pages
+          named_bar_sync(8, kConvThreads + 32);
+          rv.advance();
+          // the segment's page kVDepth ahead goes into the buffer just stored
+          if (q + kVDepth < np) load_page(v[d], bt_row, L, p0 + q + kVDepth);
+        }
+      }
+      if (stop) break;
+      g += static_cast<uint32_t>(sg.t1 - sg.t0);
+      {  // ---- this group's share of the segment epilogue
+        const uint32_t pb = (g - 1u) & 1u;  // the segment's last tile
+        // O complete; the last P message (with the final scales) landed
+        bool ok = warp_wait(bar(kOF), nseg & 1u, ctl) && warp_wait(bar(kPM + pb), ((g - 1u) >> 1) & 1u, ctl);
+        if (!named_bar_all(6, kConvThreads, ok)) break;
+        tc_fence_after();
+        epilogue_share(warp, fin_s[pb * kHeads + 32 * (warp & 3) + lane], sg, pb);
+        tc_fence_before();
+        named_bar_sync(6, kConvThreads);
+        if (ptid == 0) mbar_arrive(bar(kEpiD));
+      }
+      ++nseg;
+    }
+    if (lane == 0) bulk_wait_all();  // the output stores have completed
   } else if (!score_rank && warp < kMmaWarp) {
-    // ================================================= V conversion (value ranks, warps 4-15)
+    // ================================================= V tail zeroing (value ranks, warps 4-15, bf16 variant)
     const int ptid = threadIdx.x - 128;
     const uint32_t rVR = mapa(bar(kVR), 2);
     constexpr int kPieces = kVPage / 16;  // 2048 pieces of 16 B
@@ -909,27 +1051,10 @@ mla_decode_mtp_kernel(const __grid_constant__ DecodeParams p, const __grid_const
           }
           const uint32_t stg = vslot(rv.idx);
           const int r_end = L - j * kTileRows - e * kPage;  // rows >= r_end lie past the cache end: zero them
-          if (r_end >= kPage) {
-            if (!kBf16PV) {
-#pragma unroll 4
-              for (int piece = ptid; piece < kPieces; piece += kConvThreads) {
-                const uint32_t a = stg + 16u * piece;
-                const uint4 v = ld_shared_v4u(a);
-                st_shared_v4(a, bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z),
-                             bf16x2_to_f16x2(v.w));
-              }
-            }
-          } else {
+          if (r_end < kPage) {
             for (int piece = ptid; piece < kPieces; piece += kConvThreads) {
-              const uint32_t a = stg + 16u * piece;
               const int r = (piece & 511) >> 3;  // the swizzle only permutes pieces within a row
-              if (r >= r_end) {
-                st_shared_zero16(a);
-              } else if (!kBf16PV) {
-                const uint4 v = ld_shared_v4u(a);
-                st_shared_v4(a, bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z),
-                             bf16x2_to_f16x2(v.w));
-              }
+              if (r >= r_end) st_shared_zero16(stg + 16u * piece);
             }
           }
           fence_proxy_async_smem();

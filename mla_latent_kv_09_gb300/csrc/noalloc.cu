@@ -60,8 +60,11 @@ extern "C" int mla_decode_noalloc(const void* q, const void* kv_cache, int64_t n
                                   int batch, int s_q, int num_heads, float softmax_scale,
                                   const int32_t* topk_idx, int topk, unsigned flags, void* out, float* lse,
                                   mla_stream_t stream) {
-  if (batch < 1 || s_q < 1 || s_q > 2) return batch < 1 ? MLA_ERR_INVALID_ARG : MLA_ERR_UNSUPPORTED;
-  if (num_heads != mla::kHeads) return MLA_ERR_UNSUPPORTED;
+  // every argument check of mla_decode first: a rejected call leaves the
+  // array (and the status word an earlier call left there) untouched
+  int rc = mla::check_decode_args(q, kv_cache, num_pages, block_table, bt_stride, cache_lens, batch, s_q,
+                                  num_heads, softmax_scale, topk_idx, topk, flags, out, lse);
+  if (rc != MLA_OK) return rc;
   // the same number of work units the allocating path would use, fewer if
   // the workspace would not fit the array; reject what does not fit at all
   int err = MLA_OK;
@@ -71,8 +74,7 @@ extern "C" int mla_decode_noalloc(const void* q, const void* kv_cache, int64_t n
   const size_t need = mla::ws_layout(batch, s_q, units).total;
   if (need > kScratchBytes) return MLA_ERR_WORKSPACE;
   void* ws = nullptr;
-  int rc = scratch_address(&ws);
-  if (rc != MLA_OK) return rc;
+  if ((rc = scratch_address(&ws)) != MLA_OK) return rc;
   // nothing in the array must start at zero: the plan rewrites every metadata
   // word and the status, partials are written before they are read
   if ((rc = mla_decode_plan(cache_lens, batch, s_q, topk, units, ws, kScratchBytes, stream)) != MLA_OK) return rc;
@@ -81,4 +83,21 @@ extern "C" int mla_decode_noalloc(const void* q, const void* kv_cache, int64_t n
       MLA_OK)
     return rc;
   return mla_combine(ws, kScratchBytes, batch, s_q, num_heads, flags, units, out, lse, stream);
+}
+
+extern "C" int mla_noalloc_status(mla_stream_t stream) {
+  void* ws = nullptr;
+  const int rc = scratch_address(&ws);
+  if (rc != MLA_OK) return rc;
+  return mla_workspace_status(ws, stream);
+}
+
+extern "C" int mla_noalloc_workspace(void** dev_ptr, size_t* bytes) {
+  if (!dev_ptr || !bytes) return MLA_ERR_INVALID_ARG;
+  void* ws = nullptr;
+  const int rc = scratch_address(&ws);
+  if (rc != MLA_OK) return rc;
+  *dev_ptr = ws;
+  *bytes = kScratchBytes;
+  return MLA_OK;
 }

@@ -31,11 +31,11 @@ def _build():
 
 
 def run(w, out_fp32=True, num_units=0, validate=False, q=None, kv=None, table=None, topk_idx="same",
-        f16_pv=False):
+        bf16_pv=False):
     o, lse = m.decode_step(w.q if q is None else q, w.kv if kv is None else kv,
                            w.block_table if table is None else table, w.cache_lens, w.softmax_scale,
                            causal=w.causal, topk_idx=w.topk_idx if topk_idx == "same" else topk_idx,
-                           out_fp32=out_fp32, num_units=num_units, validate=validate, f16_pv=f16_pv)
+                           out_fp32=out_fp32, num_units=num_units, validate=validate, bf16_pv=bf16_pv)
     torch.cuda.synchronize()
     return o.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64)
 
@@ -181,22 +181,51 @@ def test_two_token_lengths_around_tile_edges(L, causal):
     assert_close(o, lse, o_ref, lse_ref)
 
 
-@pytest.mark.parametrize("f16_pv", [False, True], ids=["bf16pv", "f16pv"])
-def test_two_token_value_precision_modes(f16_pv):
+@pytest.mark.parametrize("bf16_pv", [False, True], ids=["f16pv", "bf16pv"])
+def test_two_token_value_precision_modes(bf16_pv):
     w = wl.make_config("mtp_b64", device="cuda", batch=6, length=3000)
     o_ref, lse_ref = reference(w)
-    o, lse = run(w, f16_pv=f16_pv)
+    o, lse = run(w, bf16_pv=bf16_pv)
     assert_close(o, lse, o_ref, lse_ref)
-    ob, _ = run(w, out_fp32=False, f16_pv=f16_pv)
+    ob, _ = run(w, out_fp32=False, bf16_pv=bf16_pv)
     assert_close(ob, lse, o_ref, lse_ref)
 
 
-def test_two_token_full_size_f16_pv_sampled():
+def test_two_token_full_size_bf16_pv_sampled():
     w = wl.make_config("mtp_b64", device="cuda")
     sel = [(b, t) for b in (3, 17, 40, 63) for t in range(2)]
-    o, lse = run(w, f16_pv=True)
+    o, lse = run(w, bf16_pv=True)
     o_ref, lse_ref = reference(w, select=sel)
     assert_close(o, lse, o_ref, lse_ref, select=sel)
+
+
+def test_two_token_peaked_softmax_default_mode_meets_the_bar():
+    # 5% of the cache rows scaled x8: a few keys dominate each softmax row, so
+    # the rounding of the largest weights reaches O almost unattenuated.  The
+    # default (fp16 weights and values) must meet the bar on fp32 O, and the
+    # bf16 O within its half-ulp at |O| ~ 30 as for the long-context workload.
+    w = wl.make_workload("mtp_spiked", [6000, 3000, 129], s_q=2, causal=True, spike_frac=0.05, seed=31,
+                         device="cuda")
+    o_ref, lse_ref = reference(w)
+    o, lse = run(w)
+    assert_close(o, lse, o_ref, lse_ref)
+    ob, lseb = run(w, out_fp32=False)
+    assert_close(ob, lseb, o_ref, lse_ref, bf16_scaled=True)
+
+
+def test_two_token_peaked_softmax_bf16_mode_stays_within_its_stated_error():
+    # MLA_FLAG_BF16_PV keeps 8 significant bits on the weights: on the same
+    # peaked input its O error is a few times the bar (an fp64 emulation of
+    # the kernel's rounding gives max-abs 0.03-0.05, mean-abs ~1.3e-3); the
+    # LSE does not depend on the value precision and still meets its bar
+    w = wl.make_workload("mtp_spiked", [6000, 3000, 129], s_q=2, causal=True, spike_frac=0.05, seed=31,
+                         device="cuda")
+    o_ref, lse_ref = reference(w)
+    o, lse = run(w, bf16_pv=True)
+    err = np.abs(o - o_ref)
+    assert err.max() <= 0.1 and err.mean() <= 3e-3, (err.max(), err.mean())
+    fin = np.isfinite(lse_ref)
+    assert np.abs(lse[fin] - lse_ref[fin]).max() <= LSE_MAX
 
 
 def test_two_token_split_across_units_matches_single_unit():
@@ -289,6 +318,92 @@ def test_validate_reports_bad_table_and_bad_index():
     with pytest.raises(m.MlaError) as e:
         run(ws, topk_idx=idx, validate=True)
     assert e.value.status == m.MLA_ERR_BAD_INDEX
+
+
+def test_validated_step_is_asynchronous_and_capturable():
+    # the check, the attention and the combine are recorded in a CUDA graph
+    # (no host synchronisation inside the calls); a clean replay matches the
+    # unvalidated step bit for bit; after a table entry is poisoned in place,
+    # a replay reports MLA_ERR_BAD_TABLE and leaves O and LSE unwritten
+    w = wl.make_workload("vg", [200, 300], seed=2, device="cuda")
+    dev = torch.device("cuda")
+    ws = m.Workspace(2, 1, 0, dev)
+    U = ws.num_units
+    out = torch.empty((2, 1, 128, 512), dtype=torch.float32, device=dev)
+    lse = torch.empty((2, 1, 128), dtype=torch.float32, device=dev)
+    table = w.block_table.clone()
+    flags = m.MLA_FLAG_VALIDATE | m.MLA_FLAG_OUT_FP32
+
+    def step():
+        st = torch.cuda.current_stream()
+        m.mla_decode_plan(w.cache_lens, 2, 1, 0, U, ws.buf, ws.nbytes, st)
+        m.mla_decode(w.q, w.kv, w.num_pages, table, table.stride(0), w.cache_lens, 2, 1, 128, w.softmax_scale,
+                     None, 0, flags, U, ws.buf, ws.nbytes, out, lse, st)
+        m.mla_combine(ws.buf, ws.nbytes, 2, 1, 128, flags, U, out, lse, st)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    out.fill_(float("nan"))
+    graph.replay()
+    torch.cuda.synchronize()
+    assert m.mla_workspace_status(ws.buf) == m.MLA_OK
+    o_ref, l_ref = run(w, num_units=U)
+    assert np.array_equal(out.cpu().numpy(), o_ref) and np.array_equal(lse.cpu().numpy(), l_ref)
+    table[1, 2] = w.num_pages + 5
+    out.fill_(float("nan"))
+    lse.fill_(float("nan"))
+    graph.replay()
+    torch.cuda.synchronize()
+    assert m.mla_workspace_status(ws.buf) == m.MLA_ERR_BAD_TABLE
+    assert torch.isnan(out).all() and torch.isnan(lse).all()
+
+
+def _poke_value(kv, table, b, pos, dim, value):
+    flat = kv.view(-1, 576)
+    row = int(table[b, pos // 64]) * 64 + pos % 64
+    flat[row, dim] = value
+
+
+def test_validate_reports_value_dims_that_do_not_fit_fp16():
+    w = wl.make_workload("vr", [100, 200], seed=3, device="cuda")
+    # outside what the step reads or outside the value dims: no error
+    kv = w.kv.clone()
+    _poke_value(kv, w.block_table, 1, 150, 530, 70000.0)  # a RoPE dim (scores only)
+    _poke_value(kv, w.block_table, 0, 110, 7, float("inf"))  # past request 0's 100 tokens
+    run(w, kv=kv, validate=True)
+    # a visible value dim beyond fp16's range, and a NaN one
+    for v in (70000.0, float("nan")):
+        bad = kv.clone()
+        _poke_value(bad, w.block_table, 1, 150, 7, v)
+        with pytest.raises(m.MlaError) as e:
+            run(w, kv=bad, validate=True)
+        assert e.value.status == m.MLA_ERR_VALUE_RANGE
+    # the two-token path: fp16 by default (checked), bf16 on request (no limit)
+    w2 = wl.make_workload("vr2", [100, 200], s_q=2, causal=True, seed=3, device="cuda")
+    bad = w2.kv.clone()
+    _poke_value(bad, w2.block_table, 1, 150, 7, 70000.0)
+    with pytest.raises(m.MlaError) as e:
+        run(w2, kv=bad, validate=True)
+    assert e.value.status == m.MLA_ERR_VALUE_RANGE
+    o, lse = run(w2, kv=bad, validate=True, bf16_pv=True)
+    h = wl.host_arrays(w2)
+    h_kv = wl.bf16_bits(bad)
+    o_ref, lse_ref = oracle.mla_decode(h["q_bits"], h_kv, h["block_table"], h["cache_lens"], h["softmax_scale"],
+                                       causal=True)
+    # dims 0..511 are key dims too: the poked row's scores reach ~1e4 x the
+    # scale, where fp32 accumulation of the 576-term product keeps ~5 digits,
+    # so the LSE is compared relatively; O carries up to 70000 x a weight in
+    # that dim, where the bf16 value product's relative error bound applies
+    fin = np.isfinite(lse_ref)
+    assert np.all(np.abs(lse[fin] - lse_ref[fin]) <= LSE_MAX + 4e-5 * np.abs(lse_ref[fin]))
+    assert np.all(np.abs(o - o_ref) <= O_MAX + 2.0 ** -7 * np.abs(o_ref))
 
 
 # ---------------------------------------------------------------- failure path (bounded waits)
