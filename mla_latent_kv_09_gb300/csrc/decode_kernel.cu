@@ -316,9 +316,7 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
           for (int c = 0; c < 16; ++c) pk[c] = 0u;
         } else {
           // P = 2^(s * scale_log2 - m) in one FFMA + EX2; the fp16-rounded
-          // weights are summed exactly by reading each fp16 pattern as an fp32
-          // pattern shifted by 13 bits, which is the same value times 2^-112
-          // (normal and subnormal alike); the 2^112 is applied once per tile
+          // weights are widened exactly and summed in fp32
           float zs[4] = {0.f, 0.f, 0.f, 0.f}, ze[4] = {0.f, 0.f, 0.f, 0.f};
           const float nm = -m_used;
 #pragma unroll
@@ -326,11 +324,10 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
             const float p0 = ex2_approx(fmaf(s[2 * c], p.scale_log2, nm));
             const float p1 = ex2_approx(fmaf(s[2 * c + 1], p.scale_log2, nm));
             pk[c] = pack_f16x2(p0, p1);
-            zs[c & 3] += __uint_as_float((pk[c] << 13) & 0x0fffe000u) +
-                         __uint_as_float((pk[c] >> 3) & 0x0fffe000u);
+            zs[c & 3] = add_f16x2_halves(zs[c & 3], pk[c]);
             ze[c & 3] += p0 + p1;
           }
-          z += ((zs[0] + zs[1]) + (zs[2] + zs[3])) * 5.192296858534828e33f;  // 2^112
+          z += (zs[0] + zs[1]) + (zs[2] + zs[3]);
           zx += (ze[0] + ze[1]) + (ze[2] + ze[3]);
         }
 

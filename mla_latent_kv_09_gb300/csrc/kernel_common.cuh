@@ -130,6 +130,19 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
   return pack_f16x2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
 }
 
+// acc + (both halves of a packed fp16x2 / bf16x2 word), each half widened
+// exactly to fp32 by a mixed-precision add (one instruction per half)
+__device__ __forceinline__ float add_f16x2_halves(float acc, uint32_t w) {
+  asm("{\n .reg .f16 lo, hi;\n mov.b32 {lo, hi}, %1;\n add.rn.f32.f16 %0, lo, %0;\n add.rn.f32.f16 %0, hi, %0;\n}"
+      : "+f"(acc) : "r"(w));
+  return acc;
+}
+__device__ __forceinline__ float add_bf16x2_halves(float acc, uint32_t w) {
+  asm("{\n .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %1;\n add.rn.f32.bf16 %0, lo, %0;\n add.rn.f32.bf16 %0, hi, %0;\n}"
+      : "+f"(acc) : "r"(w));
+  return acc;
+}
+
 __device__ __forceinline__ uint4 ld_shared_v4u(uint32_t a) {
   uint4 v;
   asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"

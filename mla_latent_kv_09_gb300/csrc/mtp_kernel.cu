@@ -543,10 +543,7 @@ mla_decode_mtp_kernel(const __grid_constant__ DecodeParams p, const __grid_const
 #pragma unroll
           for (int c = 0; c < 16; ++c) pk[c] = 0u;
         } else {
-          // the 16-bit weights are summed exactly: a bf16 pattern is the top
-          // half of the fp32 pattern of the same value; an fp16 pattern moved
-          // up by 13 bits is the fp32 pattern of the same value times 2^-112
-          // (normal and subnormal alike), the 2^112 is applied once per tile
+          // the 16-bit weights are widened exactly and summed in fp32
           float zs[4] = {0.f, 0.f, 0.f, 0.f}, ze[4] = {0.f, 0.f, 0.f, 0.f};
           const float nm = -m_used;
 #pragma unroll
@@ -554,14 +551,10 @@ mla_decode_mtp_kernel(const __grid_constant__ DecodeParams p, const __grid_const
             const float p0 = ex2_approx(fmaf(s[2 * c], p.scale_log2, nm));
             const float p1 = ex2_approx(fmaf(s[2 * c + 1], p.scale_log2, nm));
             pk[c] = kBf16PV ? pack_bf16x2(p0, p1) : pack_f16x2(p0, p1);
-            if (kBf16PV)
-              zs[c & 3] += __uint_as_float(pk[c] << 16) + __uint_as_float(pk[c] & 0xffff0000u);
-            else
-              zs[c & 3] += __uint_as_float((pk[c] << 13) & 0x0fffe000u) +
-                           __uint_as_float((pk[c] >> 3) & 0x0fffe000u);
+            zs[c & 3] = kBf16PV ? add_bf16x2_halves(zs[c & 3], pk[c]) : add_f16x2_halves(zs[c & 3], pk[c]);
             ze[c & 3] += p0 + p1;
           }
-          zr += ((zs[0] + zs[1]) + (zs[2] + zs[3])) * (kBf16PV ? 1.f : 5.192296858534828e33f);  // 2^112
+          zr += (zs[0] + zs[1]) + (zs[2] + zs[3]);
           zx += (ze[0] + ze[1]) + (ze[2] + ze[3]);
         }
         // ---- the local P copy: free once the previous tile's bulk copy read it
