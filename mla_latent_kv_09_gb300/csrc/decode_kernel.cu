@@ -33,9 +33,10 @@
 //
 // Warps (384 threads).  S side: 0-7 softmax (warp w: head rows 32*(w%4)..,
 // columns 32*(w/4).. of each tile), 8 MMA issue + TMEM owner, 9 TMA
-// producer, 10-11 row gather (sparse).  O side: 0-3 O correction + epilogue
-// (thread i = head row i = TMEM lane i), 4-7 V conversion (with 10-11 when
-// dense) or row gather + conversion (sparse), 8 MMA issue, 9 TMA producer.
+// producer (dense) or, with 10-11, row gather (sparse).  O side: 0-3 O
+// correction + epilogue (thread i = head row i = TMEM lane i), 4-7 and 10-11
+// V conversion (dense) or row gather + conversion (sparse), 8 MMA issue,
+// 9 TMA producer (dense).
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -178,7 +179,7 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
     for (int i = 0; i < kStages; ++i) {
       mbar_init(bar(kKF + i), 1);
       mbar_init(bar(kKE + i), 1);
-      mbar_init(bar(kVR + i), kSparse ? 128 : kConvThreads);
+      mbar_init(bar(kVR + i), kConvThreads);
     }
     mbar_init(bar(kQF), 1);
     for (int i = 0; i < 2; ++i) {
@@ -482,6 +483,7 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
           const uint32_t sb = g & 1u, ph = (g >> 1) & 1u;
           if (s_side) {
             if (!(ok = wait_bar<false>(bar(kKF + rs.idx), rs.phase, ctl))) break;
+            if (kSparse) fence_proxy_async_smem();  // rows written by the gather threads' copies
             if (!(ok = wait_bar<false>(bar(kSE + sb), ph ^ 1u, ctl))) break;
             tc_fence_after();
             // 36 MMAs (K = 576 in steps of 16): descriptors differ from the
@@ -528,7 +530,7 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
       drain_bar(bar(kMmaDone), 0);
     }
     __syncwarp();
-  } else if (warp == 9) {
+  } else if (warp == 9 && !kSparse) {
     // ================================================= TMA producer (whole warp; lane 0 issues)
     // S side: per segment three Q slots, then (dense) one slot per tile.  O
     // side (dense): one slot per tile, value dims only.  Page ids are read 32
@@ -589,12 +591,14 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
   } else {
     // ================================================= O side warps 4-7 (+10-11 dense): V conversion
     // (dense) or gather + conversion (sparse); S side warps 10-11: gather (sparse)
-    const int ptid = s_side ? threadIdx.x - 320 : (warp < 8 ? threadIdx.x - 128 : threadIdx.x - 192);
+    // dense: O side warps 4-7, 10-11 convert (ptid 0..191); sparse: S side
+    // warps 9-11 (ptid 0..95) and O side warps 4-7, 10-11 (0..191) gather
+    const int ptid = s_side ? threadIdx.x - 288 : (warp < 8 ? threadIdx.x - 128 : threadIdx.x - 192);
     SegIter it(p, unit);
     Seg sg;
     Ring3 rs;
     bool ok = true;
-    if ((!kSparse && s_side) || (kSparse && !s_side && warp >= 10)) {
+    if ((!kSparse && s_side) || (kSparse && !s_side && warp == 9)) {
       // nothing to do: the S side consumes TMA tiles as they land
     } else if (!kSparse) {
       // ---- O side, dense: 192 threads convert the landed bf16 value tile to fp16 in place
@@ -635,13 +639,38 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
         }
       }
     } else {
-      // ---- sparse: each S-side thread gathers one row (all 576 dims), each
-      // pair of O-side threads one row's 512 value dims (which they then
-      // convert to fp16 in place); rows the list does not name are zero-filled
-      const int nthreads = s_side ? 64 : 128;
-      const int r = s_side ? ptid : (ptid >> 1);
-      const int pc0 = s_side ? 0 : (ptid & 1) * 32;          // first 16-byte piece of the row
-      const int npc = s_side ? kNumChunks * 8 : 32;           // pieces this thread moves
+      // ---- sparse: rows named by the index list are gathered with 16-byte
+      // cp.async copies, one row at a time per warp so that a warp's copies
+      // read contiguous bytes (a lane per 16-byte piece): on the S side three
+      // warps (all 576 dims), on the O side six (the 512 value dims, which
+      // they then convert to fp16 in place); warp w of n takes rows w, w + n,
+      // ...  Rows the list does not name (or that lie outside the pool) are
+      // zero-filled.  Each lane looks up one row's pool position, a tile
+      // ahead, and the warp shares them by shuffles.  Nothing waits for a
+      // tile's copies where they are issued: on the S side the tile's landing
+      // barrier tracks every gather thread's copies (the MMA thread then
+      // orders them before its tensor-core reads); on the O side a warp
+      // converts tile j - 1 after issuing tile j's copies.
+      const int nthreads = s_side ? 96 : kConvThreads;
+      const int nw = nthreads / 32;
+      const int gw = ptid >> 5;                          // gather warp 0 .. nw - 1
+      const int rows_w = (kPage - gw + nw - 1) / nw;     // rows gw, gw + nw, ... of a tile
+      const int npc = s_side ? kNumChunks * 8 : 64;      // 16-byte pieces per row
+      // O side: convert the pieces this lane brought into stage `st`
+      auto convert_own = [&](uint32_t st) {
+        for (int i = 0; i < rows_w; ++i) {
+          const int r = gw + nw * i;
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            const int c16 = lane + 32 * k;
+            const uint32_t a = st + (c16 >> 3) * kChunkBytes + r * 128 + (((c16 & 7) ^ (r & 7)) << 4);
+            const uint4 v = ld_shared_v4u(a);
+            st_shared_v4(a, bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z),
+                         bf16x2_to_f16x2(v.w));
+          }
+        }
+      };
+      int pend = -1;  // O side: stage index of the tile whose copies are still in flight
       while (ok && it.next(sg)) {
         if (s_side) {  // three Q slots (TMA, issued by one gather thread)
           const int qy = (sg.b * p.s_q + tok) * kHeads;
@@ -660,49 +689,63 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
         const long long bt_row = static_cast<long long>(sg.b) * p.s_q + tok;
         const int* idx = p.topk_idx + bt_row * p.topk;
         const int* tbl = p.block_table + static_cast<long long>(sg.b) * p.bt_stride;
+        // this lane's row of the warp's share of tile j: its pool row, or -1
+        auto lookup = [&](int j) -> long long {
+          long long pr = -1;
+          if (lane < rows_w) {
+            const int pos = j * 64 + gw + nw * lane;
+            if (pos < p.topk) {
+              const int ix = __ldg(idx + pos);
+              if (ix >= 0 && ix < L && (ix >> 6) < p.bt_stride) {
+                const int pg = __ldg(tbl + (ix >> 6));
+                if (pg >= 0 && pg < p.num_pages) pr = static_cast<long long>(pg) * kPage + (ix & 63);
+              }
+            }
+          }
+          return pr;
+        };
+        long long my_row = lookup(sg.t0);
         for (int j = sg.t0; j < sg.t1; ++j, rs.advance()) {
-          if (!(ok = warp_wait(bar(kKE + rs.idx), rs.phase ^ 1u, ctl))) break;
-          long long prow = -1;
-          const int pos = j * 64 + r;
-          if (pos < p.topk) {
-            const int ix = idx[pos];
-            if (ix >= 0 && ix < L && (ix >> 6) < p.bt_stride) {
-              const int pg = tbl[ix >> 6];
-              if (pg >= 0 && pg < p.num_pages) prow = static_cast<long long>(pg) * kPage + (ix & 63);
-            }
-          }
+          ok = warp_wait(bar(kKE + rs.idx), rs.phase ^ 1u, ctl);
+          // the S side's gather warps meet at a named barrier below: they vote
+          // here so that all leave if any wait ran out
+          if (s_side) ok = named_bar_all(5, nthreads, ok);
+          if (!ok) break;
           const uint32_t stg = sStage + rs.idx * stage_bytes;
-          const uint16_t* src = p.kv + (prow >= 0 ? prow : 0) * kDqk;
-          const uint32_t src_bytes = prow >= 0 ? 16u : 0u;  // 0: the copy writes zeros
-#pragma unroll 8
-          for (int c = 0; c < npc; ++c) {
-            const int c16 = pc0 + c;
-            cp_async_16_zfill(stg + (c16 >> 3) * kChunkBytes + r * 128 + (((c16 & 7) ^ (r & 7)) << 4),
-                              src + c16 * 8, src_bytes);
+          for (int i = 0; i < rows_w; ++i) {
+            const long long prow = __shfl_sync(0xffffffffu, my_row, i);
+            const int r = gw + nw * i;
+            const uint16_t* src = p.kv + (prow >= 0 ? prow : 0) * kDqk;
+            const uint32_t src_bytes = prow >= 0 ? 16u : 0u;  // 0: the copy writes zeros
+            for (int c16 = lane; c16 < npc; c16 += 32)
+              cp_async_16_zfill(stg + (c16 >> 3) * kChunkBytes + r * 128 + (((c16 & 7) ^ (r & 7)) << 4),
+                                src + c16 * 8, src_bytes);
           }
-          cp_async_commit();
-          cp_async_wait<0>();
-          if (!s_side) {  // convert the pieces this thread brought in
-#pragma unroll 8
-            for (int c = 0; c < npc; ++c) {
-              const int c16 = pc0 + c;
-              const uint32_t a = stg + (c16 >> 3) * kChunkBytes + r * 128 + (((c16 & 7) ^ (r & 7)) << 4);
-              uint4 v;
-              asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                           : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a) : "memory");
-              st_shared_v4(a, bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z),
-                           bf16x2_to_f16x2(v.w));
-            }
-          }
-          fence_proxy_async_smem();
+          if (j + 1 < sg.t1) my_row = lookup(j + 1);  // its latency overlaps the copies and the next wait
           if (s_side) {
-            named_bar_sync(5, nthreads);
+            cp_async_mbar_track(bar(kKF + rs.idx));
+            named_bar_sync(5, nthreads);  // every thread's copies are tracked before the one arrival
             if (ptid == 0) mbar_arrive(bar(kKF + rs.idx));
           } else {
-            mbar_arrive(bar(kVR + rs.idx));
+            cp_async_commit();
+            if (pend >= 0) {  // the previous tile: landed -> fp16 -> ready for the value product
+              cp_async_wait<1>();
+              convert_own(sStage + pend * stage_bytes);
+              fence_proxy_async_smem();
+              mbar_arrive(bar(kVR + pend));
+            }
+            pend = static_cast<int>(rs.idx);
           }
         }
+        if (!s_side && pend >= 0 && ok) {  // the segment's last tile
+          cp_async_wait<0>();
+          convert_own(sStage + pend * stage_bytes);
+          fence_proxy_async_smem();
+          mbar_arrive(bar(kVR + pend));
+          pend = -1;
+        }
       }
+      cp_async_wait<0>();  // no copy outlives the CTA
     }
   }
 

@@ -247,6 +247,12 @@ __device__ __forceinline__ void cp_async_16_zfill(uint32_t dst, const void* src,
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Make the mbarrier track this thread's prior cp.async copies: its current
+// phase cannot complete before they have landed.  Net zero on the pending
+// arrival count (the barrier still needs its ordinary arrivals).
+__device__ __forceinline__ void cp_async_mbar_track(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
