@@ -31,12 +31,12 @@
 // partial plus its LSE, merged by the combine kernel (the split-K remedy of
 // "The 31-Millisecond Smoking Gun").
 //
-// Warps (384 threads).  S side: 0-7 softmax (warp w: head rows 32*(w%4)..,
-// columns 32*(w/4).. of each tile), 8 MMA issue + TMEM owner, 9 TMA
-// producer (dense) or, with 10-11, row gather (sparse).  O side: 0-3 O
-// correction + epilogue (thread i = head row i = TMEM lane i), 4-7 and 10-11
-// V conversion (dense) or row gather + conversion (sparse), 8 MMA issue,
-// 9 TMA producer (dense).
+// Warps (384 threads dense, 512 top-k).  S side: 0-7 softmax (warp w: head
+// rows 32*(w%4).., columns 32*(w/4).. of each tile), 8 MMA issue + TMEM
+// owner, 9 TMA producer (dense) or, with 10-15, row gather (top-k).  O side:
+// 0-3 O correction + epilogue (thread i = head row i = TMEM lane i), 4-7 and
+// 10-11 V conversion (dense) or 4-7 and 10-15 row gather + conversion
+// (top-k), 8 MMA issue, 9 TMA producer (dense).
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -73,8 +73,11 @@ constexpr uint32_t kColS = 0;     // S side: two 64-column score buffers
 constexpr uint32_t kColQ = 128;   // S side: Q, 288 columns (576 bf16 packed in pairs)
 constexpr uint32_t kColO = 0;     // O side: O, 512 columns
 
-constexpr int kThreads = 384;       // 12 warps
-constexpr int kConvThreads = 192;   // O side, dense: warps 4-7 and 10-11 convert V
+constexpr int kThreads = 384;       // 12 warps (dense); the top-k variant has 16
+constexpr int kThreadsSparse = 512;
+// O side: warps 4-7 and 10-11 convert V (dense); warps 4-7 and 10-15 gather
+// and convert it (top-k)
+__host__ __device__ constexpr int conv_threads(bool sparse) { return sparse ? 320 : 192; }
 constexpr float kRescaleLog2 = 8.0f;
 
 enum Bar {
@@ -133,7 +136,7 @@ __host__ __device__ constexpr uint32_t p_message_bytes(bool last) {
 }
 
 template <bool kSparse>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kSparse ? kThreadsSparse : kThreads, 1)
 mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tm_q,
                   const __grid_constant__ CUtensorMap tm_kv) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -179,7 +182,7 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
     for (int i = 0; i < kStages; ++i) {
       mbar_init(bar(kKF + i), 1);
       mbar_init(bar(kKE + i), 1);
-      mbar_init(bar(kVR + i), kConvThreads);
+      mbar_init(bar(kVR + i), conv_threads(kSparse));
     }
     mbar_init(bar(kQF), 1);
     for (int i = 0; i < 2; ++i) {
@@ -592,7 +595,7 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
     // ================================================= O side warps 4-7 (+10-11 dense): V conversion
     // (dense) or gather + conversion (sparse); S side warps 10-11: gather (sparse)
     // dense: O side warps 4-7, 10-11 convert (ptid 0..191); sparse: S side
-    // warps 9-11 (ptid 0..95) and O side warps 4-7, 10-11 (0..191) gather
+    // warps 9-15 (ptid 0..223) and O side warps 4-7, 10-15 (0..319) gather
     const int ptid = s_side ? threadIdx.x - 288 : (warp < 8 ? threadIdx.x - 128 : threadIdx.x - 192);
     SegIter it(p, unit);
     Seg sg;
@@ -611,7 +614,7 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
           const int r_end = L - j * 64;  // rows >= r_end lie past the cache end: zero them
           if (r_end >= 64) {
 #pragma unroll 4
-            for (int piece = ptid; piece < kPieces; piece += kConvThreads) {
+            for (int piece = ptid; piece < kPieces; piece += conv_threads(false)) {
               const uint32_t a = stg + 16u * piece;
               uint4 v;
               asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -620,7 +623,7 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
                            bf16x2_to_f16x2(v.w));
             }
           } else {
-            for (int piece = ptid; piece < kPieces; piece += kConvThreads) {
+            for (int piece = ptid; piece < kPieces; piece += conv_threads(false)) {
               const uint32_t a = stg + 16u * piece;
               const int r = (piece & 511) >> 3;  // the swizzle only permutes pieces within a row
               if (r >= r_end) {
@@ -641,8 +644,8 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
     } else {
       // ---- sparse: rows named by the index list are gathered with 16-byte
       // cp.async copies, one row at a time per warp so that a warp's copies
-      // read contiguous bytes (a lane per 16-byte piece): on the S side three
-      // warps (all 576 dims), on the O side six (the 512 value dims, which
+      // read contiguous bytes (a lane per 16-byte piece): on the S side seven
+      // warps (all 576 dims), on the O side ten (the 512 value dims, which
       // they then convert to fp16 in place); warp w of n takes rows w, w + n,
       // ...  Rows the list does not name (or that lie outside the pool) are
       // zero-filled.  Each lane looks up one row's pool position, a tile
@@ -651,7 +654,7 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
       // barrier tracks every gather thread's copies (the MMA thread then
       // orders them before its tensor-core reads); on the O side a warp
       // converts tile j - 1 after issuing tile j's copies.
-      const int nthreads = s_side ? 96 : kConvThreads;
+      const int nthreads = s_side ? 224 : conv_threads(true);
       const int nw = nthreads / 32;
       const int gw = ptid >> 5;                          // gather warp 0 .. nw - 1
       const int rows_w = (kPage - gw + nw - 1) / nw;     // rows gw, gw + nw, ... of a tile
@@ -761,7 +764,7 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
 
 // ------------------------------------------------------------------ host side
 int decode_smem_bytes() { return kSmemBytes; }
-int decode_threads(bool) { return kThreads; }
+int decode_threads(bool sparse) { return sparse ? kThreadsSparse : kThreads; }
 
 cudaError_t decode_set_attrs() {
   cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
