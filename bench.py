@@ -373,7 +373,7 @@ def run_ours(args, world, rank, local):
 
     # the other workloads first (one at a time, freed after), the headline last
     others = {}
-    extra = [c for c in (args.also or "").split(",") if c and c != args.config]
+    extra = [c for c in (args.also or "").split(",") if c and c not in (args.config, "none")]
     for name in extra:
         w = wl.make_config(name, seed=args.seed + rank, device=dev)
         r = time_step(m, w, args, dev, world)
@@ -391,7 +391,7 @@ def run_ours(args, world, rank, local):
         del w, r
         torch.cuda.empty_cache()
 
-    w = wl.make_config(args.config, seed=args.seed + rank, device=dev)
+    w = wl.make_config(args.config, seed=args.seed + rank, device=dev, batch=args.batch, length=args.length)
     B, s_q = w.batch, w.s_q
     sampler = ClockSampler(local)
     r = time_step(m, w, args, dev, world, sampler=sampler)
@@ -444,7 +444,8 @@ def run_ours(args, world, rank, local):
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_ms_max, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": args.config, "batch": B, "s_q": s_q, "heads": 128, "d_qk": 576, "d_v": 512,
+        "config": {"workload": args.config + ("" if args.batch is None and args.length is None else " (reduced)"),
+                   "batch": B, "s_q": s_q, "heads": 128, "d_qk": 576, "d_v": 512,
                    "page": 64, "causal": w.causal, "topk": w.topk, "num_units": r["num_units"],
                    "value_product": "bf16 P and V" if args.bf16_pv else "fp16 P and V",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
@@ -477,6 +478,10 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="mtp_b64")
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--batch", type=int, default=None,
+                    help="shrink the headline workload to this many requests (profiling runs)")
+    ap.add_argument("--length", type=int, default=None,
+                    help="shrink the headline workload's cache length (profiling runs)")
     ap.add_argument("--num-units", type=int, default=0)
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-e2e", action="store_true")
@@ -490,7 +495,7 @@ def main():
     ap.add_argument("--cpu-budget-other", type=float, default=4.0,
                     help="seconds of oracle work for each other workload's CPU baseline")
     ap.add_argument("--also", default="single,uniform_b32,long_b128,sparse_b80",
-                    help="other workloads timed before the headline one (comma-separated; '' for none)")
+                    help="other workloads timed before the headline one (comma-separated; 'none' for none)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -236,11 +236,13 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
     float* xmax = reinterpret_cast<float*>(smem + kOffXchg);               // [2 parity][2 half][128]
     float* xsum = reinterpret_cast<float*>(smem + kOffXchg + 4 * kHeads * 4);  // [2 half][2][128]
     const int pair_bar = 1 + q4;  // named barrier of the two warps of this quarter
+    // the two warps of a quarter meet at named barriers: they vote there, so
+    // that a wait that ran out in one of them makes both leave
     SegIter it(p, unit);
     Seg sg;
     uint32_t g = 0, nseg = 0;
-    bool ok = true;
-    while (ok && it.next(sg)) {
+    bool ok = true, stop = false;  // ok: this warp's waits so far; stop: the quarter leaves
+    while (!stop && it.next(sg)) {
       const int L = max(p.cache_lens[sg.b], 0);
       const int vis = p.causal ? L - p.s_q + tok + 1 : L;
       const long long bt_row = static_cast<long long>(sg.b) * p.s_q + tok;
@@ -252,18 +254,21 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
       for (int j = sg.t0; j < sg.t1; ++j, ++g) {
         const uint32_t sb = g & 1u, ph = (g >> 1) & 1u;
         const bool last = (j == sg.t1 - 1);
-        if (!(ok = warp_wait(bar(kSF + sb), ph, ctl))) break;
-        tc_fence_after();
+        ok = ok && warp_wait(bar(kSF + sb), ph, ctl);
         float s[32];
-        {
+        if (ok) {
+          tc_fence_after();
           uint32_t r[32];
           tmem_ld32(tmem + lane_base + kColS + 64u * sb + 32u * half, r);
           tmem_wait_ld();
 #pragma unroll
           for (int c = 0; c < 32; ++c) s[c] = __uint_as_float(r[c]);
+          tc_fence_before();
+          mbar_arrive(bar(kSE + sb));
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) s[c] = NEG_INF;
         }
-        tc_fence_before();
-        mbar_arrive(bar(kSE + sb));
 
         // ---- mask (masked scores become -inf), then the row max of the raw
         // scores over both halves (the scale is positive, so max commutes with it)
@@ -303,7 +308,10 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
         }
         float* xm = xmax + (sb * 2) * kHeads;
         xm[half * kHeads + row] = mh;
-        named_bar_sync(pair_bar, 64);
+        if (!named_bar_all(pair_bar, 64, ok)) {
+          stop = true;
+          break;
+        }
         const float mt = fmaxf(mh, xm[(half ^ 1) * kHeads + row]) * p.scale_log2;  // same in both halves
 
         // ---- online softmax with a lazy rescale of the reference max
@@ -336,20 +344,25 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
         }
 
         // ---- P message to the O side, once it is done with this slot
-        if (!(ok = warp_wait(bar(kPFree + sb), ph ^ 1u, ctl))) break;
+        ok = ok && warp_wait(bar(kPFree + sb), ph ^ 1u, ctl);
         const uint32_t mbar = rPM + 8u * sb;
-        const uint32_t prow = rP + sb * kPBytes;
+        if (ok) {
+          const uint32_t prow = rP + sb * kPBytes;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint32_t piece = static_cast<uint32_t>(4 * half + k);
-          st_async_v4(prow + ((piece ^ (row & 7)) << 4), pk[4 * k], pk[4 * k + 1], pk[4 * k + 2],
-                      pk[4 * k + 3], mbar);
+          for (int k = 0; k < 4; ++k) {
+            const uint32_t piece = static_cast<uint32_t>(4 * half + k);
+            st_async_v4(prow + ((piece ^ (row & 7)) << 4), pk[4 * k], pk[4 * k + 1], pk[4 * k + 2],
+                        pk[4 * k + 3], mbar);
+          }
+          if (half == 0) st_async_b32(rAlpha + sb * kHeads * 4u, __float_as_uint(alpha), mbar);
         }
-        if (half == 0) st_async_b32(rAlpha + sb * kHeads * 4u, __float_as_uint(alpha), mbar);
         if (last) {  // ---- segment end: both halves' sums -> final scale and LSE
           xsum[(half * 2 + 0) * kHeads + row] = z;
           xsum[(half * 2 + 1) * kHeads + row] = zx;
-          named_bar_sync(pair_bar, 64);
+          if (!named_bar_all(pair_bar, 64, ok)) {
+            stop = true;
+            break;
+          }
           if (half == 0) {
             const float zt = z + xsum[(2 + 0) * kHeads + row];
             const float zxt = zx + xsum[(2 + 1) * kHeads + row];
@@ -362,7 +375,10 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
               p.part_lse[(static_cast<long long>(sg.slot) * p.s_q + tok) * kHeads + row] = lse;
             }
           }
-          named_bar_sync(pair_bar, 64);  // xsum is reused at the next segment end
+          if (!named_bar_all(pair_bar, 64, ok)) {  // xsum is reused at the next segment end
+            stop = true;
+            break;
+          }
         }
       }
       ++nseg;
