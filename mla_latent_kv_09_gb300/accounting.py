@@ -54,3 +54,30 @@ def step_bytes(cache_lens, s_q: int, causal: bool, topk_idx=None, out_bytes_per_
         extra = 0
     per_qt = H * D_QK * 2 + H * D_V * out_bytes_per_elem + H * 4
     return int(rows * ROW_BYTES + B * s_q * per_qt + 4 * table + extra + 4 * B)
+
+
+# Weight-absorption BMMs on either side of the attention ("DeepSeek V3/R1
+# Inference Efficiency (2)", §2.4.1, Compute): the query side maps each head's
+# 128 "nope" dims into the 512-dim latent space through W_UK, the output side
+# maps the 512-dim head output back to 128 dims through W_UV.  T tokens are
+# (request, query token) pairs.
+D_NOPE = 128
+
+
+def absorb_q_flops(num_tokens: int) -> int:
+    return 2 * H * num_tokens * D_NOPE * D_V
+
+
+def absorb_o_flops(num_tokens: int) -> int:
+    return 2 * H * num_tokens * D_V * D_NOPE
+
+
+def absorb_q_bytes(num_tokens: int, with_pe: bool = True) -> int:
+    """q_nope in, W_UK, the 512 latent dims out (plus the 64 RoPE dims copied)."""
+    pe = 2 * num_tokens * H * (D_QK - D_V) * 2 if with_pe else 0
+    return num_tokens * H * D_NOPE * 2 + H * D_V * D_NOPE * 2 + num_tokens * H * D_V * 2 + pe
+
+
+def absorb_o_bytes(num_tokens: int) -> int:
+    """O in, W_UV, O' out."""
+    return num_tokens * H * D_V * 2 + H * D_V * D_NOPE * 2 + num_tokens * H * D_NOPE * 2

@@ -1,4 +1,5 @@
-"""Plain fp64 CPU oracle for absorbed-MLA decode attention.
+"""Plain fp64 CPU oracle for absorbed-MLA decode attention and the
+weight-absorption BMMs on either side of it.
 
 TEST INFRASTRUCTURE ONLY.  Nothing in the product path (the CUDA library, its
 Python binding, the timed legs of the benchmark) may import or call this
@@ -19,3 +20,4 @@ from .mla_oracle import (  # noqa: F401
     softmax_weights,
     visible_positions,
 )
+from .absorb_oracle import absorb_o, absorb_q  # noqa: F401,E402
