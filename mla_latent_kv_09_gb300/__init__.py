@@ -8,7 +8,9 @@ kernels); this package is its Python face:
   * `decode_step`, which allocates the outputs and runs plan -> decode ->
     combine on the current stream;
   * `decode_step_host`, the same call for host-resident inputs (copies in,
-    runs, copies the outputs back).
+    runs, copies the outputs back);
+  * `absorb_q` / `absorb_o`, the weight-absorption BMMs on either side of
+    the attention (query through W_UK, output through W_UV).
 
 PyTorch is used only to allocate device memory and to name streams.
 """
@@ -33,6 +35,8 @@ from ._binding import (  # noqa: F401
     SIGNATURES,
     MlaError,
     load,
+    mla_absorb_o,
+    mla_absorb_q,
     mla_combine,
     mla_decode,
     mla_decode_noalloc,
@@ -138,3 +142,58 @@ def decode_step_host(q, kv_cache, block_table, cache_lens, softmax_scale: float,
     lse_host.copy_(l, non_blocking=True)
     torch.cuda.current_stream(device).synchronize()
     return out_host, lse_host
+
+
+def _rows(t, dims: int, name: str) -> int:
+    """Row stride of a token-major [T, H, dims] activation whose rows may be
+    spaced wider than `dims` (e.g. a slice of a [T, H, 192] tensor)."""
+    if t.dim() != 3 or t.shape[2] != dims or t.stride(2) != 1 or t.stride(0) != t.shape[1] * t.stride(1):
+        raise ValueError(f"{name}: expected [T, H, {dims}] with unit stride in the last dim and rows "
+                         "evenly spaced over (token, head)")
+    return t.stride(1)
+
+
+def absorb_q(q_nope, w_uk, q_pe=None, *, out=None, status=None, stream=None):
+    """Query-side absorption: q_latent[t, h] = W_UK[h] @ q_nope[t, h].
+
+    q_nope [T, H, 128] bf16 (rows may be strided, e.g. [..., :128] of a
+    [T, H, 192] projection output), w_uk [H, 512, 128] bf16, q_pe [T, H, 64]
+    bf16 with the same row stride, or None.  Returns `out`, by default a new
+    [T, H, 576] tensor (the decode attention's query) with the RoPE dims in
+    512..575, or [T, H, 512] without q_pe.  `status` (int32 device tensor,
+    one element) receives MLA_ERR_TIMEOUT if a device wait runs out.
+    """
+    import torch
+    T, H = q_nope.shape[0], q_nope.shape[1]
+    q_stride = _rows(q_nope, 128, "q_nope")
+    if q_pe is not None and _rows(q_pe, 64, "q_pe") != q_stride:
+        raise ValueError("q_pe must have the row stride of q_nope")
+    if out is None:
+        out = torch.empty((T, H, D_QK if q_pe is not None else D_V), dtype=torch.bfloat16, device=q_nope.device)
+    out_stride = _rows(out, out.shape[2], "out")
+    if status is None:
+        status = torch.zeros(1, dtype=torch.int32, device=q_nope.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q_nope.device)
+    mla_absorb_q(q_nope, q_pe, q_stride, w_uk, T, H, out, out_stride, status, stream)
+    return out
+
+
+def absorb_o(o, w_uv, *, out=None, status=None, stream=None):
+    """Output-side absorption: out[t, h] = O[t, h] @ W_UV[h].
+
+    o [T, H, 512] bf16 (the decode attention's output), w_uv [H, 512, 128]
+    bf16.  Returns `out`, by default a new [T, H, 128] bf16 tensor.
+    """
+    import torch
+    T, H = o.shape[0], o.shape[1]
+    o_stride = _rows(o, 512, "o")
+    if out is None:
+        out = torch.empty((T, H, 128), dtype=torch.bfloat16, device=o.device)
+    out_stride = _rows(out, 128, "out")
+    if status is None:
+        status = torch.zeros(1, dtype=torch.int32, device=o.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(o.device)
+    mla_absorb_o(o, o_stride, w_uv, T, H, out, out_stride, status, stream)
+    return out

@@ -30,7 +30,7 @@ MLA_FLAG_OUT_FP32 = 2
 MLA_FLAG_VALIDATE = 4
 MLA_FLAG_BF16_PV = 8
 
-# every symbol include/mla_decode.h declares: name -> (restype, argtypes)
+# every symbol include/mla_decode.h and include/mla_absorb.h declare: name -> (restype, argtypes)
 _c_int, _c_size, _vp, _i64, _f32, _uint = (ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p,
                                            ctypes.c_int64, ctypes.c_float, ctypes.c_uint)
 SIGNATURES = {
@@ -48,6 +48,8 @@ SIGNATURES = {
     "mla_noalloc_status": (_c_int, [_vp]),
     "mla_noalloc_workspace": (_c_int, [ctypes.POINTER(_vp), ctypes.POINTER(_c_size)]),
     "mla_status_string": (ctypes.c_char_p, [_c_int]),
+    "mla_absorb_q": (_c_int, [_vp, _vp, _i64, _vp, _c_int, _c_int, _vp, _i64, _vp, _vp]),
+    "mla_absorb_o": (_c_int, [_vp, _i64, _vp, _c_int, _c_int, _vp, _i64, _vp, _vp]),
 }
 
 _lib = None
@@ -184,3 +186,17 @@ def mla_noalloc_workspace():
     ptr, n = ctypes.c_void_p(), ctypes.c_size_t()
     _check("mla_noalloc_workspace", load().mla_noalloc_workspace(ctypes.byref(ptr), ctypes.byref(n)))
     return ptr.value, n.value
+
+
+def mla_absorb_q(q_nope, q_pe, q_stride: int, w_uk, num_tokens: int, num_heads: int, out, out_stride: int,
+                 status, stream=None) -> None:
+    _check("mla_absorb_q", load().mla_absorb_q(
+        _ptr(q_nope), _ptr(q_pe), int(q_stride), _ptr(w_uk), int(num_tokens), int(num_heads), _ptr(out),
+        int(out_stride), _ptr(status), _stream(stream)))
+
+
+def mla_absorb_o(o, o_stride: int, w_uv, num_tokens: int, num_heads: int, out, out_stride: int, status,
+                 stream=None) -> None:
+    _check("mla_absorb_o", load().mla_absorb_o(
+        _ptr(o), int(o_stride), _ptr(w_uv), int(num_tokens), int(num_heads), _ptr(out), int(out_stride),
+        _ptr(status), _stream(stream)))

@@ -2,8 +2,8 @@
 
 TEST INFRASTRUCTURE.  Only tests, the smoke check and the benchmark's
 CPU-baseline leg may use it; it shares no code with the GPU path.  Every step
-is the definition written out in float64 with a library matmul (einsum), no
-blocking or reordering.
+is the page's bmm written out in float64 with a library batched matmul
+(numpy.matmul over the head axis), no blocking or reordering.
 
 What it computes ("DeepSeek V3/R1 Inference Efficiency (2): Reverse-
 Engineering the Production Deployment", §2.4.1, Compute):
@@ -46,7 +46,8 @@ def absorb_q(q_nope_bits: np.ndarray, w_uk_bits: np.ndarray) -> np.ndarray:
     w = bf16_bits_to_f64(np.asarray(w_uk_bits))
     if q.ndim != 3 or w.ndim != 3 or q.shape[1] != w.shape[0] or q.shape[2] != w.shape[2]:
         raise ValueError("expected q_nope [T, H, d] and W_UK [H, c, d]")
-    return np.einsum("thd,hcd->thc", q, w)
+    # bmm([H, T, d], [H, d, c]) = Q'' @ W_UK^T per head, back to [T, H, c]
+    return np.matmul(q.transpose(1, 0, 2), w.transpose(0, 2, 1)).transpose(1, 0, 2)
 
 
 def absorb_o(o_bits: np.ndarray, w_uv_bits: np.ndarray) -> np.ndarray:
@@ -55,4 +56,5 @@ def absorb_o(o_bits: np.ndarray, w_uv_bits: np.ndarray) -> np.ndarray:
     w = bf16_bits_to_f64(np.asarray(w_uv_bits))
     if o.ndim != 3 or w.ndim != 3 or o.shape[1] != w.shape[0] or o.shape[2] != w.shape[1]:
         raise ValueError("expected O [T, H, c] and W_UV [H, c, d]")
-    return np.einsum("thc,hcd->thd", o, w)
+    # bmm([H, T, c], [H, c, d]) per head, back to [T, H, d]
+    return np.matmul(o.transpose(1, 0, 2), w).transpose(1, 0, 2)

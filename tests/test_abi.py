@@ -11,11 +11,12 @@ import mla_latent_kv_09_gb300 as m
 from mla_latent_kv_09_gb300 import build as mbuild
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "mla_decode.h")
+HEADERS = [os.path.join(ROOT, "include", f) for f in sorted(os.listdir(os.path.join(ROOT, "include")))
+           if f.endswith(".h")]
 
 
 def declared_functions():
-    text = open(HEADER).read()
+    text = "\n".join(open(h).read() for h in HEADERS)
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(mla_\w+)\s*\(", text, flags=re.M)
     return sorted(set(names))
@@ -31,7 +32,7 @@ def test_header_declares_the_three_calls_and_helpers():
     names = declared_functions()
     for n in ["mla_decode_plan", "mla_decode", "mla_combine", "mla_decode_workspace_size",
               "mla_status_string", "mla_default_num_units", "mla_decode_plan_host",
-              "mla_workspace_status", "mla_selftest_wait_timeout"]:
+              "mla_workspace_status", "mla_selftest_wait_timeout", "mla_absorb_q", "mla_absorb_o"]:
         assert n in names
 
 
@@ -83,6 +84,28 @@ def test_null_pointers_and_bad_shapes_are_rejected_before_any_launch(lib):
     assert lib.mla_selftest_wait_timeout(None, 1 << 20, None) == m.MLA_ERR_INVALID_ARG
     assert lib.mla_selftest_wait_timeout(ok_ptr, 64, None) == m.MLA_ERR_INVALID_ARG  # smaller than the header
     assert lib.mla_selftest_wait_timeout(ok_ptr + 16, 1 << 20, None) == m.MLA_ERR_INVALID_ARG  # misaligned
+
+
+def test_absorption_calls_check_their_arguments_on_the_host(lib):
+    ok = 1 << 20
+    q = [ok, ok + 256, 192, ok, 128, 128, ok, 576, ok, None]  # q_nope, q_pe, q_stride, w_uk, T, H, out, out_stride, status
+    o = [ok, 512, ok, 128, 128, ok, 128, ok, None]            # o, o_stride, w_uv, T, H, out, out_stride, status
+    for f, good, bad in [
+        (lib.mla_absorb_q, q, [(0, None), (3, None), (6, None), (8, None), (0, ok + 8), (1, ok + 8),
+                               (8, ok + 2), (2, 120), (2, 196), (7, 512), (7, 580), (4, -1)]),
+        (lib.mla_absorb_o, o, [(0, None), (2, None), (5, None), (7, None), (0, ok + 8), (5, ok + 4),
+                               (1, 504), (1, 516), (6, 120), (3, -1)]),
+    ]:
+        for i, v in bad:
+            a = list(good); a[i] = v
+            assert f(*a) == m.MLA_ERR_INVALID_ARG, (f.__name__, i, v)
+        for h in (0, 129):  # head counts outside 1..128
+            a = list(good); a[5 if f is lib.mla_absorb_q else 4] = h
+            assert f(*a) == m.MLA_ERR_UNSUPPORTED
+    # without the RoPE rows the output may be 512 wide; zero tokens launch
+    # nothing (MLA_ERR_DEVICE where no GPU is present)
+    a = list(q); a[1] = None; a[7] = 512; a[4] = 0
+    assert lib.mla_absorb_q(*a) in (m.MLA_OK, m.MLA_ERR_DEVICE)
 
 
 def test_python_binding_raises_when_library_missing(tmp_path):

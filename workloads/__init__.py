@@ -68,8 +68,8 @@ def _np_rng(seed: int, stream: int) -> np.random.Generator:
     return np.random.Generator(np.random.Philox(np.random.SeedSequence([seed, stream])))
 
 
-def _randn_bf16(shape, seed: int, stream: int, device) -> torch.Tensor:
-    """N(0,1) rounded to bf16, drawn in fixed chunks on `device`."""
+def _randn_bf16(shape, seed: int, stream: int, device, scale: float = 1.0) -> torch.Tensor:
+    """N(0, scale^2) rounded to bf16, drawn in fixed chunks on `device`."""
     out = torch.empty(shape, dtype=torch.bfloat16, device=device)
     flat = out.view(-1)
     g = torch.Generator(device=device)
@@ -77,8 +77,8 @@ def _randn_bf16(shape, seed: int, stream: int, device) -> torch.Tensor:
     n = flat.numel()
     for lo in range(0, n, _CHUNK_ELEMS):
         hi = min(n, lo + _CHUNK_ELEMS)
-        flat[lo:hi] = torch.randn(hi - lo, generator=g, device=device,
-                                  dtype=torch.float32).to(torch.bfloat16)
+        x = torch.randn(hi - lo, generator=g, device=device, dtype=torch.float32)
+        flat[lo:hi] = (x if scale == 1.0 else x * scale).to(torch.bfloat16)
     return out
 
 
@@ -192,3 +192,38 @@ def host_arrays(w: Workload):
         block_table=w.block_table.cpu().numpy(), cache_lens=w.cache_lens.cpu().numpy(),
         softmax_scale=w.softmax_scale, causal=w.causal,
         topk_idx=None if w.topk_idx is None else w.topk_idx.cpu().numpy())
+
+
+# ---------------------------------------------------------------- absorption BMMs
+D_NOPE, D_ROPE = 128, 64
+
+
+@dataclasses.dataclass
+class AbsorbInputs:
+    q_proj: torch.Tensor  # bf16 [T, H, 192]: per head 128 "nope" dims, then 64 RoPE dims
+    o: torch.Tensor       # bf16 [T, H, 512]: an attention output in the latent space
+    w_uk: torch.Tensor    # bf16 [H, 512, 128]
+    w_uv: torch.Tensor    # bf16 [H, 512, 128]
+
+    @property
+    def q_nope(self) -> torch.Tensor:
+        return self.q_proj[..., :D_NOPE]
+
+    @property
+    def q_pe(self) -> torch.Tensor:
+        return self.q_proj[..., D_NOPE:]
+
+
+def make_absorb(num_tokens: int, num_heads: int = H, seed: int = 0, device="cpu") -> AbsorbInputs:
+    """Inputs of the two weight-absorption BMMs for a step of `num_tokens`
+    (request, query token) pairs ("DeepSeek V3/R1 Inference Efficiency (2)",
+    §2.4.1: q_nope [n_head, bs, 128], W_UK and W_UV [n_head, 512, 128]).
+    Activations are N(0,1); weights are random-init N(0, 1/fan_in) (fan_in =
+    128 for W_UK, whose contraction runs over d, 512 for W_UV, over c), so
+    that both outputs are O(1).  The query projection output is one
+    [T, H, 192] tensor, as the query up-projection produces it."""
+    q = _randn_bf16((num_tokens, num_heads, D_NOPE + D_ROPE), seed, 20, device)
+    o = _randn_bf16((num_tokens, num_heads, D_V), seed, 21, device)
+    w_uk = _randn_bf16((num_heads, D_V, D_NOPE), seed, 22, device, scale=1.0 / math.sqrt(D_NOPE))
+    w_uv = _randn_bf16((num_heads, D_V, D_NOPE), seed, 23, device, scale=1.0 / math.sqrt(D_V))
+    return AbsorbInputs(q_proj=q, o=o, w_uk=w_uk, w_uv=w_uv)
