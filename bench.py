@@ -11,7 +11,9 @@ Before the headline workload the same step is timed on the four other
 decode workloads (one request of 256 tokens; B=32 at 4096 tokens; B=128 at
 32768 tokens with 5% of rows x8; B=80 top-2048 of 65536), each with its
 roofline figures and a bounded oracle sample on the host cores, reported
-under `other_workloads`.
+under `other_workloads`.  The weight-absorption BMMs either side of the
+attention (query through W_UK, output through W_UV) are timed alone at the
+headline step's 128 tokens and at 64 tokens, under `absorb`.
 
 Prints ONE JSON line.  `value` is the whole-job attention throughput in
 TFLOP/s (algorithmic FLOPs of every rank's steps / max-over-ranks time);
@@ -358,6 +360,151 @@ def roofline_of(w, r, pk, pk_kind, step_ms):
     }
 
 
+ABSORB_SOURCES = ["absorb_kernel.cu", "kernel_common.cuh", "common.cuh", "ptx.cuh"]
+
+
+def absorb_hash() -> str:
+    h = hashlib.sha256()
+    for f in ABSORB_SOURCES:
+        h.update(open(os.path.join(ROOT, "mla_latent_kv_09_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def absorb_traffic(kernel: str, tokens: int):
+    """DRAM bytes per launch of an absorption kernel from a committed ncu
+    capture on the current source (else None)."""
+    path = os.path.join(ROOT, "profiles", "absorb_traffic.json")
+    if not os.path.exists(path):
+        return None
+    e = json.load(open(path)).get(f"{kernel}/T{tokens}")
+    if not e or e.get("kernel_hash") != absorb_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+def time_absorb(m, args, dev, tokens: int, pk, pk_kind, with_cpu: bool):
+    """The weight-absorption BMMs around the attention for one step of
+    `tokens` (request, query token) pairs, 128 heads: each call timed alone
+    with CUDA events, 256 MB of L2 flushed before every launch (the inputs,
+    ~40 MB, would otherwise stay in L2)."""
+    import torch
+
+    import workloads as wl
+    from mla_latent_kv_09_gb300 import accounting as acc
+
+    inp = wl.make_absorb(tokens, seed=args.seed, device=dev)
+    q_out = torch.empty((tokens, 128, 576), dtype=torch.bfloat16, device=dev)
+    o_out = torch.empty((tokens, 128, 128), dtype=torch.bfloat16, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    calls = {
+        "q": (lambda: m.absorb_q(inp.q_nope, inp.w_uk, inp.q_pe, out=q_out, status=status, stream=stream),
+              acc.absorb_q_flops(tokens), acc.absorb_q_bytes(tokens), "mla_absorb_q_kernel"),
+        "o": (lambda: m.absorb_o(inp.o, inp.w_uv, out=o_out, status=status, stream=stream),
+              acc.absorb_o_flops(tokens), acc.absorb_o_bytes(tokens), "mla_absorb_o_kernel"),
+    }
+    res = {"tokens": tokens, "heads": 128}
+    n = max(args.steps, 20)
+    for key, (fn, flops, nbytes, kname) in calls.items():
+        for _ in range(max(args.warmup, 3)):
+            flush.zero_()
+            fn()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        torch.cuda.synchronize()
+        for a, b in ev:
+            flush.zero_()
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize()
+        us = sum(a.elapsed_time(b) for a, b in ev) / n * 1e3
+        gbs = nbytes / (us * 1e-6) / 1e9
+        res[key] = {"us": us, "gflop": flops / 1e9, "algorithmic_mb": nbytes / 1e6, "tflops": flops / (us * 1e-6) / 1e12,
+                    "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                                 "frac": gbs / pk["hbm_gbs"], "traffic": absorb_traffic(kname, tokens),
+                                 "kernel": kname, "peak_source": f"{pk_kind} (burst)"}}
+    if m.mla_workspace_status(status, stream.cuda_stream) != 0:
+        raise RuntimeError("absorption kernels reported a device status")
+    if with_cpu:
+        import oracle
+        t0 = time.perf_counter()
+        oracle.absorb_q(wl.bf16_bits(inp.q_nope.contiguous()), wl.bf16_bits(inp.w_uk))
+        oracle.absorb_o(wl.bf16_bits(inp.o), wl.bf16_bits(inp.w_uv))
+        dt = time.perf_counter() - t0
+        res["cpu_baseline"] = {"value": dt * 1e6, "unit": "us for both calls", "cores": torch.get_num_threads(),
+                               "kind": "oracle", "sample": f"both calls once at {tokens} tokens (fp64, numpy matmul)"}
+    del inp, q_out, o_out, flush
+    torch.cuda.empty_cache()
+    return res
+
+
+def time_layer(m, w, args, dev, ws):
+    """The attention block of one decode step as a serving loop runs it: query
+    absorption (writing the attention's query in place), plan, attention,
+    combine and output absorption, recorded once in a CUDA graph and replayed
+    with 256 MB of L2 flushed before every replay.  Random-init W_UK / W_UV
+    of the model's shapes; the query projection output is synthetic."""
+    import torch
+
+    import workloads as wl
+
+    B, s_q = w.batch, w.s_q
+    T = B * s_q
+    inp = wl.make_absorb(T, seed=args.seed + 1, device=dev)
+    q = torch.empty((B, s_q, 128, 576), dtype=torch.bfloat16, device=dev)
+    out = torch.empty((B, s_q, 128, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, s_q, 128), dtype=torch.float32, device=dev)
+    o_proj_in = torch.empty((T, 128, 128), dtype=torch.bfloat16, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flags = (m.MLA_FLAG_CAUSAL if w.causal else 0) | (m.MLA_FLAG_BF16_PV if args.bf16_pv else 0)
+    U = ws.num_units
+
+    def block():
+        st = torch.cuda.current_stream(dev)
+        m.absorb_q(inp.q_nope, inp.w_uk, inp.q_pe, out=q.view(T, 128, 576), status=status, stream=st)
+        m.mla_decode_plan(w.cache_lens, B, s_q, w.topk, U, ws.buf, ws.nbytes, st)
+        m.mla_decode(q, w.kv, w.num_pages, w.block_table, w.block_table.stride(0), w.cache_lens, B, s_q, 128,
+                     w.softmax_scale, w.topk_idx, w.topk, flags, U, ws.buf, ws.nbytes, out, lse, st)
+        m.mla_combine(ws.buf, ws.nbytes, B, s_q, 128, flags, U, out, lse, st)
+        m.absorb_o(out.view(T, 128, 512), inp.w_uv, out=o_proj_in, status=status, stream=st)
+
+    stream = torch.cuda.current_stream(dev)
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        block()
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    ref = o_proj_in.clone()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        block()
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        graph.replay()
+    n = max(args.steps, 20)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    torch.cuda.synchronize()
+    for a, b in ev:
+        flush.zero_()
+        a.record(stream)
+        graph.replay()
+        b.record(stream)
+    torch.cuda.synchronize()
+    if m.mla_workspace_status(status, stream.cuda_stream) != 0 or m.mla_workspace_status(ws.buf, stream.cuda_stream):
+        raise RuntimeError("attention block: a kernel reported a device status")
+    if not torch.equal(o_proj_in, ref):
+        raise RuntimeError("attention block: graph replays changed the output")
+    us = sum(a.elapsed_time(b) for a, b in ev) / n * 1e3
+    del inp, q, out, lse, o_proj_in, flush
+    torch.cuda.empty_cache()
+    return {"us_per_call": us, "tokens": T,
+            "launch": "CUDA graph of absorb_q, plan, decode, combine, absorb_o (programmatic dependent launches)",
+            "l2": "256 MB L2 flush before every replay"}
+
+
 def run_ours(args, world, rank, local):
     import torch
 
@@ -391,11 +538,22 @@ def run_ours(args, world, rank, local):
         del w, r
         torch.cuda.empty_cache()
 
+    # the absorption BMMs either side of the attention, at the headline
+    # step's 128 tokens (64 requests x 2) and at the pages' bs = 64
+    absorb = None
+    if not args.no_absorb:
+        absorb = {f"T{t}": time_absorb(m, args, dev, t, pk, pk_kind, rank == 0 and world == 1
+                                       and not args.no_cpu_baseline) for t in (128, 64)}
+        absorb["page_context"] = ("H800 estimates at bs=64 (context only): 10 us for the query-side and 8 us "
+                                  "for the output-side BMM")
+
     w = wl.make_config(args.config, seed=args.seed + rank, device=dev, batch=args.batch, length=args.length)
     B, s_q = w.batch, w.s_q
     sampler = ClockSampler(local)
     r = time_step(m, w, args, dev, world, sampler=sampler)
     clocks = sampler.stop()
+    if absorb is not None:
+        absorb["layer"] = time_layer(m, w, args, dev, r["ws"])
     step_ms_max = max_over_ranks(r["step_ms"], world)
     rf = roofline_of(w, r, pk, pk_kind, step_ms_max)
     flops = rf["flops"]
@@ -466,6 +624,7 @@ def run_ours(args, world, rank, local):
         "cpu_baseline": cpu,
         "wall_s_timed_region": r["wall_s"],
         "other_workloads": others,
+        "absorb": absorb,
     }
     print(json.dumps(line), flush=True)
 
@@ -490,6 +649,8 @@ def main():
     ap.add_argument("--bf16-pv", action="store_true",
                     help="two-token dense path: value product with bf16 P and V (MLA_FLAG_BF16_PV)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-absorb", action="store_true",
+                    help="skip timing the weight-absorption BMMs around the attention")
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of oracle work for the headline workload's CPU baseline")
     ap.add_argument("--cpu-budget-other", type=float, default=4.0,

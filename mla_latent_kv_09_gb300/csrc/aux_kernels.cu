@@ -115,7 +115,8 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(const int* __restrict_
                                                           const float* __restrict__ part_lse,
                                                           const float* __restrict__ part_o, int s_q,
                                                           int out_fp32, void* out, float* lse) {
-  grid_dependency_wait();  // the decode kernel has finished (programmatic dependent launch)
+  grid_launch_dependents();  // a kernel launched after this one may set up (it waits for this grid)
+  grid_dependency_wait();    // the decode kernel has finished (programmatic dependent launch)
   if (hdr[kHdrStatus] != 0) return;  // a failed check or wait: the step's outputs stay unwritten
   const int bt = blockIdx.x;
   const int b = bt / s_q, t = bt - b * s_q;
