@@ -9,9 +9,10 @@ every timed step.
 
 Before the headline workload the same step is timed on the four other
 decode workloads (one request of 256 tokens; B=32 at 4096 tokens; B=128 at
-32768 tokens with 5% of rows x8; B=80 top-2048 of 65536), each with its
-roofline figures and a bounded oracle sample on the host cores, reported
-under `other_workloads`.  The weight-absorption BMMs either side of the
+32768 tokens with 5% of rows x8; B=80 top-2048 of 65536) and on the B=64
+requests with four causal query tokens (mtp4_b64), each with its roofline
+figures and a bounded oracle sample on the host cores, reported under
+`other_workloads`.  The weight-absorption BMMs either side of the
 attention (query through W_UK, output through W_UV) are timed alone at the
 headline step's 128 tokens and at 64 tokens, under `absorb`.
 
@@ -655,7 +656,7 @@ def main():
                     help="seconds of oracle work for the headline workload's CPU baseline")
     ap.add_argument("--cpu-budget-other", type=float, default=4.0,
                     help="seconds of oracle work for each other workload's CPU baseline")
-    ap.add_argument("--also", default="single,uniform_b32,long_b128,sparse_b80",
+    ap.add_argument("--also", default="single,uniform_b32,long_b128,sparse_b80,mtp4_b64",
                     help="other workloads timed before the headline one (comma-separated; 'none' for none)")
     args = ap.parse_args()
     if args.warmup < 3:

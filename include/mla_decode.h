@@ -79,7 +79,7 @@ typedef enum {
 } mla_status;
 
 enum {
-  MLA_FLAG_CAUSAL = 1,   /* s_q = 2 MTP decode: token t sees [0, len - s_q + t] */
+  MLA_FLAG_CAUSAL = 1,   /* s_q >= 2 (MTP decode): token t sees [0, len - s_q + t] */
   MLA_FLAG_OUT_FP32 = 2, /* O is written as fp32 instead of bf16           */
   MLA_FLAG_VALIDATE = 4, /* check lengths, table, indices and value range
                             first; see mla_decode                           */
@@ -94,7 +94,7 @@ enum {
                             below 65504 in magnitude                        */
 };
 
-enum { MLA_NUM_HEADS = 128, MLA_D_QK = 576, MLA_D_V = 512, MLA_PAGE = 64 };
+enum { MLA_NUM_HEADS = 128, MLA_D_QK = 576, MLA_D_V = 512, MLA_PAGE = 64, MLA_MAX_SQ = 8 };
 
 /*
  * Number of persistent work units that `num_units = 0` selects on the
@@ -102,7 +102,9 @@ enum { MLA_NUM_HEADS = 128, MLA_D_QK = 576, MLA_D_V = 512, MLA_PAGE = 64 };
  * cluster, and the count is the number of co-resident 2-CTA clusters.
  * s_q = 2: a dense unit is a 4-CTA cluster (two SM pairs) serving both query
  * tokens, a top-k unit is two 2-CTA clusters (one per token); the count is
- * what both forms keep resident.  Host-only; returns 0 and sets *err on
+ * what both forms keep resident.  s_q = 3 .. MLA_MAX_SQ: a unit is s_q 2-CTA
+ * clusters, one per token (each token's cluster reads the request's pages;
+ * the repeats are served by L2).  Host-only; returns 0 and sets *err on
  * failure (err may be NULL).
  */
 int mla_default_num_units(int s_q, int* err);
@@ -110,7 +112,7 @@ int mla_default_num_units(int s_q, int* err);
 /*
  * Bytes of workspace the three calls need.  Pure host arithmetic.
  *   batch      requests (>= 1)
- *   s_q        query tokens per request (1 or 2)
+ *   s_q        query tokens per request (1 .. MLA_MAX_SQ)
  *   num_heads  must be 128
  *   num_units  work units per query token; 0 = mla_default_num_units(s_q)
  * Returns 0 on invalid arguments.
@@ -157,7 +159,8 @@ int mla_decode_plan_host(const int32_t* cache_lens_host, int batch, int s_q,
  *                0 .. ceil(len_b / 64) - 1 are read
  *   bt_stride    elements between block-table rows (>= ceil(max len / 64))
  *   cache_lens   int32 [batch]
- *   s_q          1, or 2 (with MLA_FLAG_CAUSAL for MTP decode)
+ *   s_q          1 .. MLA_MAX_SQ (with MLA_FLAG_CAUSAL for MTP decode:
+ *                the request's last s_q cached tokens are its query tokens)
  *   num_heads    must be 128
  *   softmax_scale  multiplies the 576-dim dot product (used as float32)
  *   topk_idx     NULL for dense attention; else int32 [batch, s_q, topk] of

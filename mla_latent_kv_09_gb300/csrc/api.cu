@@ -184,7 +184,7 @@ int mla_default_num_units(int s_q, int* err) {
   const int rc = device_state(&st);
   if (err) *err = rc;
   if (rc != MLA_OK) return 0;
-  if (s_q < 1 || s_q > 2) {
+  if (s_q < 1 || s_q > MLA_MAX_SQ) {
     if (err) *err = MLA_ERR_UNSUPPORTED;
     return 0;
   }
@@ -196,7 +196,7 @@ int mla_default_num_units(int s_q, int* err) {
 }
 
 size_t mla_decode_workspace_size(int batch, int s_q, int num_heads, int num_units) {
-  if (batch < 1 || s_q < 1 || s_q > 2 || num_heads != kHeads) return 0;
+  if (batch < 1 || s_q < 1 || s_q > MLA_MAX_SQ || num_heads != kHeads) return 0;
   int units = 0;
   if (resolve_units(s_q, num_units, &units) != MLA_OK) return 0;
   return ws_layout(batch, s_q, units).total;
@@ -205,7 +205,7 @@ size_t mla_decode_workspace_size(int batch, int s_q, int num_heads, int num_unit
 int mla_decode_plan(const int32_t* cache_lens, int batch, int s_q, int topk, int num_units, void* workspace,
                     size_t ws_bytes, mla_stream_t stream) {
   if (!cache_lens || !workspace || batch < 1 || topk < 0) return MLA_ERR_INVALID_ARG;
-  if (s_q < 1 || s_q > 2) return MLA_ERR_UNSUPPORTED;
+  if (s_q < 1 || s_q > MLA_MAX_SQ) return MLA_ERR_UNSUPPORTED;
   if (!aligned(workspace, 256)) return MLA_ERR_INVALID_ARG;
   DeviceState* st = nullptr;
   int rc = device_state(&st);
@@ -225,7 +225,7 @@ int mla_decode_plan_host(const int32_t* lens, int batch, int s_q, int topk, int 
                          int32_t* req_meta) {
   if (!lens || !unit_meta || !req_meta || batch < 1 || topk < 0 || num_units < 1 || num_units > kMaxUnits)
     return MLA_ERR_INVALID_ARG;
-  if (s_q < 1 || s_q > 2) return MLA_ERR_UNSUPPORTED;
+  if (s_q < 1 || s_q > MLA_MAX_SQ) return MLA_ERR_UNSUPPORTED;
   const int tile_rows = plan_tile_rows(s_q, topk);
   int total = 0;
   for (int b = 0; b < batch; ++b) {
@@ -264,7 +264,7 @@ int mla::check_decode_args(const void* q, const void* kv_cache, int64_t num_page
   if ((topk_idx == nullptr) != (topk == 0)) return MLA_ERR_INVALID_ARG;
   if (flags & ~static_cast<unsigned>(MLA_FLAG_CAUSAL | MLA_FLAG_OUT_FP32 | MLA_FLAG_VALIDATE | MLA_FLAG_BF16_PV))
     return MLA_ERR_INVALID_ARG;
-  if (num_heads != kHeads || s_q < 1 || s_q > 2) return MLA_ERR_UNSUPPORTED;
+  if (num_heads != kHeads || s_q < 1 || s_q > MLA_MAX_SQ) return MLA_ERR_UNSUPPORTED;
   if (!std::isfinite(softmax_scale) || !(softmax_scale > 0.f)) return MLA_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(out, 16) || !aligned(lse, 4) ||
       !aligned(block_table, 4) || !aligned(cache_lens, 4) || (topk_idx && !aligned(topk_idx, 4)))
@@ -366,7 +366,7 @@ int mla_combine(void* workspace, size_t ws_bytes, int batch, int s_q, int num_he
   if (!workspace || !out || !lse || batch < 1) return MLA_ERR_INVALID_ARG;
   if (flags & ~static_cast<unsigned>(MLA_FLAG_CAUSAL | MLA_FLAG_OUT_FP32 | MLA_FLAG_VALIDATE | MLA_FLAG_BF16_PV))
     return MLA_ERR_INVALID_ARG;
-  if (num_heads != kHeads || s_q < 1 || s_q > 2) return MLA_ERR_UNSUPPORTED;
+  if (num_heads != kHeads || s_q < 1 || s_q > MLA_MAX_SQ) return MLA_ERR_UNSUPPORTED;
   if (!aligned(out, 16) || !aligned(lse, 4) || !aligned(workspace, 256)) return MLA_ERR_INVALID_ARG;
   DeviceState* st = nullptr;
   int rc = device_state(&st);
@@ -423,7 +423,7 @@ const char* mla_status_string(int status) {
   switch (status) {
     case MLA_OK: return "MLA_OK";
     case MLA_ERR_INVALID_ARG: return "MLA_ERR_INVALID_ARG: null pointer, bad size or misaligned buffer";
-    case MLA_ERR_UNSUPPORTED: return "MLA_ERR_UNSUPPORTED: shape or mode not supported (128 heads, 576/512 dims, s_q 1..2)";
+    case MLA_ERR_UNSUPPORTED: return "MLA_ERR_UNSUPPORTED: shape or mode not supported (128 heads, 576/512 dims, s_q 1..8)";
     case MLA_ERR_WORKSPACE: return "MLA_ERR_WORKSPACE: workspace too small";
     case MLA_ERR_CUDA: return "MLA_ERR_CUDA: a CUDA call failed";
     case MLA_ERR_DEVICE: return "MLA_ERR_DEVICE: current device is not compute capability 10.3";

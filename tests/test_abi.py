@@ -69,7 +69,7 @@ def test_null_pointers_and_bad_shapes_are_rejected_before_any_launch(lib):
     assert f(*a) == m.MLA_ERR_INVALID_ARG
     a = list(args); a[8] = 64
     assert f(*a) == m.MLA_ERR_UNSUPPORTED
-    a = list(args); a[7] = 3
+    a = list(args); a[7] = 9  # s_q beyond MLA_MAX_SQ
     assert f(*a) == m.MLA_ERR_UNSUPPORTED
     a = list(args); a[0] = ok_ptr + 8  # q not 16-byte aligned
     assert f(*a) == m.MLA_ERR_INVALID_ARG

@@ -258,6 +258,54 @@ def test_two_token_sparse_uses_per_token_lists():
     assert_close(o, lse, o_ref, lse_ref)
 
 
+# ---------------------------------------------------------------- more than two query tokens (s_q = 3 .. 8)
+
+@pytest.mark.parametrize("s_q", [3, 4, 8])
+def test_multi_token_causal_lengths_around_tile_edges(s_q):
+    # lengths below s_q leave the first tokens with nothing visible (O = 0,
+    # LSE = -inf); the others end around page edges
+    lens = [1, 2, s_q, s_q + 1, 63, 64, 65, 64 + s_q, 700]
+    w = wl.make_workload(f"mtp{s_q}", lens, s_q=s_q, causal=True, seed=60 + s_q, device="cuda")
+    o_ref, lse_ref = reference(w)
+    o, lse = run(w)
+    assert_close(o, lse, o_ref, lse_ref)
+    ob, _ = run(w, out_fp32=False)
+    assert_close(ob, lse, o_ref, lse_ref)
+
+
+def test_multi_token_without_causal_mask():
+    w = wl.make_workload("mtp3nc", [5, 129, 1000], s_q=3, causal=False, seed=70, device="cuda")
+    o_ref, lse_ref = reference(w)
+    o, lse = run(w)
+    assert_close(o, lse, o_ref, lse_ref)
+
+
+def test_multi_token_sparse_uses_per_token_lists():
+    w = wl.make_workload("s4", [3000, 1500, 70], s_q=4, topk=256, pad_range=(0, 40), seed=71, device="cuda")
+    o_ref, lse_ref = reference(w)
+    o, lse = run(w)
+    assert_close(o, lse, o_ref, lse_ref)
+
+
+def test_multi_token_split_across_units_matches_single_unit():
+    w = wl.make_workload("mtp4s", [4000, 37, 2500], s_q=4, causal=True, seed=72, device="cuda")
+    o_ref, lse_ref = reference(w)
+    o1, l1 = run(w, num_units=1)
+    assert_close(o1, l1, o_ref, lse_ref)
+    o2, l2 = run(w)
+    assert_close(o2, l2, o_ref, lse_ref)
+
+
+def test_multi_token_full_size_sampled():
+    # 64 requests of U{1..8192} cached tokens, four query tokens each
+    lens = np.random.default_rng(73).integers(1, 8193, size=64)
+    w = wl.make_workload("mtp4_b64", lens, s_q=4, causal=True, seed=73, device="cuda", max_pages=128)
+    sel = [(b, t) for b in (0, 21, 42, 63) for t in range(4)]
+    o, lse = run(w)
+    o_ref, lse_ref = reference(w, select=sel)
+    assert_close(o, lse, o_ref, lse_ref, select=sel)
+
+
 # ---------------------------------------------------------------- invariants
 
 def test_page_permutation_gives_identical_output():

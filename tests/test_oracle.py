@@ -253,6 +253,19 @@ def test_two_token_causal_matches_single_token_calls():
     assert np.array_equal(o2[:, :1], o_first) and np.array_equal(l2[:, :1], l_first)
 
 
+@pytest.mark.parametrize("s_q", [3, 4])
+def test_multi_token_causal_matches_single_token_calls(s_q):
+    # token t of an s_q-token causal step attends exactly like a one-token
+    # step over the first L - s_q + t + 1 cached tokens
+    rng = np.random.default_rng(40 + s_q)
+    L = 66
+    q, kv, table, lens = _tiny_case(rng, 1, s_q, 3, [L])
+    o, l = oracle.mla_decode(q, kv, table, lens, SCALE, causal=True)
+    for t in range(s_q):
+        o1, l1 = oracle.mla_decode(q[:, t:t + 1], kv, table, lens - (s_q - 1 - t), SCALE)
+        assert np.array_equal(o[:, t:t + 1], o1) and np.array_equal(l[:, t:t + 1], l1)
+
+
 def test_sparse_full_list_equals_dense_and_is_order_free():
     rng = np.random.default_rng(25)
     L = 90

@@ -155,6 +155,8 @@ def make_config(name: str, seed: int = 0, device="cpu", batch: int | None = None
     long_b128    B=128, every L=32768, 5% of pool rows scaled x8
     sparse_b80   B=80, every L=65536, top-2048 sorted distinct positions with
                  the last 0..300 entries padded with -1
+    mtp4_b64     (beyond the five) mtp_b64's requests with four causal query
+                 tokens each: speculative decoding with three draft tokens
     """
     if name == "single":
         return make_workload(name, [length or 256], shuffle=False, seed=seed, device=device)
@@ -166,6 +168,12 @@ def make_config(name: str, seed: int = 0, device="cpu", batch: int | None = None
         top = length or 8192
         lens = _np_rng(seed, 6).integers(1, top + 1, size=B)
         return make_workload(name, lens, s_q=2, causal=True, seed=seed, device=device,
+                             max_pages=(top + PAGE - 1) // PAGE)
+    if name == "mtp4_b64":
+        B = batch or 64
+        top = length or 8192
+        lens = _np_rng(seed, 6).integers(1, top + 1, size=B)
+        return make_workload(name, lens, s_q=4, causal=True, seed=seed, device=device,
                              max_pages=(top + PAGE - 1) // PAGE)
     if name == "long_b128":
         B = batch or 128
