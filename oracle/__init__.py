@@ -1,5 +1,6 @@
-"""Plain fp64 CPU oracle for absorbed-MLA decode attention and the
-weight-absorption BMMs on either side of it.
+"""Plain fp64 CPU oracle for absorbed-MLA decode attention, the
+weight-absorption BMMs on either side of it, and the sparse-attention
+indexer (token scores, top-k lists).
 
 TEST INFRASTRUCTURE ONLY.  Nothing in the product path (the CUDA library, its
 Python binding, the timed legs of the benchmark) may import or call this
@@ -21,3 +22,4 @@ from .mla_oracle import (  # noqa: F401
     visible_positions,
 )
 from .absorb_oracle import absorb_o, absorb_q  # noqa: F401,E402
+from .indexer_oracle import indexer_scores, indexer_topk, topk_select, topk_select_fast  # noqa: F401,E402
