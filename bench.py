@@ -14,7 +14,9 @@ requests with four causal query tokens (mtp4_b64), each with its roofline
 figures and a bounded oracle sample on the host cores, reported under
 `other_workloads`.  The weight-absorption BMMs either side of the
 attention (query through W_UK, output through W_UV) are timed alone at the
-headline step's 128 tokens and at 64 tokens, under `absorb`.
+headline step's 128 tokens and at 64 tokens, under `absorb`; the
+sparse-attention indexer (scores + top-2048 lists) on the sparse workload's
+shape under `indexer`.
 
 Prints ONE JSON line.  `value` is the whole-job attention throughput in
 TFLOP/s (algorithmic FLOPs of every rank's steps / max-over-ranks time);
@@ -440,6 +442,95 @@ def time_absorb(m, args, dev, tokens: int, pk, pk_kind, with_cpu: bool):
     return res
 
 
+def time_indexer(m, args, dev, pk, pk_kind, with_cpu: bool):
+    """The sparse-attention indexer on the sparse workload's shape (80
+    requests of 65,536 cached tokens, one query token, top-2048): index
+    scores, then the top-k lists, each timed alone with CUDA events and 256 MB
+    of L2 flushed before every launch; the pair as one graph."""
+    import numpy as np
+    import torch
+
+    import workloads as wl
+    from mla_latent_kv_09_gb300 import accounting as acc
+
+    w = wl.make_config("sparse_b80", seed=args.seed, device=dev)
+    ix = wl.make_indexer(w, seed=args.seed)
+    k = 2048
+    B, s_q = w.batch, w.s_q
+    max_len = w.block_table.shape[1] * 64
+    scores = torch.empty((B, s_q, max_len), dtype=torch.float32, device=dev)
+    lists = torch.empty((B, s_q, k), dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def f_scores():
+        m.indexer_scores(ix.q_idx, ix.w_idx, ix.k_cache, w.block_table, w.cache_lens, scores=scores,
+                         status=status, stream=torch.cuda.current_stream(dev))
+
+    def f_topk():
+        m.topk_indices(scores, w.cache_lens, k, out=lists, status=status, stream=torch.cuda.current_stream(dev))
+
+    def timed(fn, n):
+        for _ in range(max(args.warmup, 3)):
+            flush.zero_()
+            fn()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        torch.cuda.synchronize()
+        for a, b in ev:
+            flush.zero_()
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in ev) / n * 1e3
+
+    n = max(min(args.steps, 200), 20)
+    us_s = timed(f_scores, n)
+    us_k = timed(f_topk, n)
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        f_scores(); f_topk()
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(graph):
+        f_scores(); f_topk()
+    us_g = timed(graph.replay, n)
+    if m.mla_workspace_status(status, stream.cuda_stream) != 0:
+        raise RuntimeError("indexer: a kernel reported a device status")
+    lens = w.cache_lens.cpu().numpy()
+    nbytes = acc.indexer_bytes(lens, s_q, False, k)
+    key_bytes = int(lens.sum()) * 256
+    gbs = key_bytes / (us_s * 1e-6) / 1e9
+    res = {"workload": "sparse_b80 shape: 80 x 65536 cached tokens, 64 index heads x 128 dims, top-2048",
+           "us_scores": us_s, "us_topk": us_k, "us_per_call": us_g,
+           "algorithmic_mb": nbytes / 1e6, "gflop": acc.indexer_flops(lens, s_q, False) / 1e9,
+           "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                        "frac": gbs / pk["hbm_gbs"], "traffic": None, "kernel": "mla_indexer_scores_kernel",
+                        "scope": "scores kernel alone: index-key bytes / its event time",
+                        "peak_source": f"{pk_kind} (burst)"},
+           "frac_roofline_call": nbytes / (pk["hbm_gbs"] * 1e9) / (us_g * 1e-6),
+           "launch": "scores and top-k each timed alone; us_per_call = CUDA graph of both"}
+    if with_cpu:
+        from oracle import indexer_oracle as io
+        # request 0's own pages only (the whole pool would not fit the host as fp64)
+        pages0 = w.block_table[0].long()
+        kc = wl.bf16_bits(ix.k_cache[pages0])
+        table0 = np.arange(pages0.numel(), dtype=np.int32)[None, :]
+        q, wt = wl.bf16_bits(ix.q_idx[:1]), ix.w_idx[:1].cpu().numpy()
+        t0 = time.perf_counter()
+        io.indexer_topk(q, wt, kc, table0, lens[:1], k)
+        dt = time.perf_counter() - t0
+        res["cpu_baseline"] = {"value": dt * 1e6 * B, "unit": "us per call (one request timed, x 80)",
+                               "cores": torch.get_num_threads(), "kind": "oracle",
+                               "sample": "indexer scores + top-2048 of one request of 65536 tokens (fp64 numpy)"}
+    del w, ix, scores, lists, flush
+    torch.cuda.empty_cache()
+    return res
+
+
 def time_layer(m, w, args, dev, ws):
     """The attention block of one decode step as a serving loop runs it: query
     absorption (writing the attention's query in place), plan, attention,
@@ -548,6 +639,10 @@ def run_ours(args, world, rank, local):
         absorb["page_context"] = ("H800 estimates at bs=64 (context only): 10 us for the query-side and 8 us "
                                   "for the output-side BMM")
 
+    indexer = None
+    if not args.no_indexer:
+        indexer = time_indexer(m, args, dev, pk, pk_kind, rank == 0 and world == 1 and not args.no_cpu_baseline)
+
     w = wl.make_config(args.config, seed=args.seed + rank, device=dev, batch=args.batch, length=args.length)
     B, s_q = w.batch, w.s_q
     sampler = ClockSampler(local)
@@ -626,6 +721,7 @@ def run_ours(args, world, rank, local):
         "wall_s_timed_region": r["wall_s"],
         "other_workloads": others,
         "absorb": absorb,
+        "indexer": indexer,
     }
     print(json.dumps(line), flush=True)
 
@@ -650,6 +746,8 @@ def main():
     ap.add_argument("--bf16-pv", action="store_true",
                     help="two-token dense path: value product with bf16 P and V (MLA_FLAG_BF16_PV)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-indexer", action="store_true",
+                    help="skip timing the sparse-attention indexer (scores + top-k)")
     ap.add_argument("--no-absorb", action="store_true",
                     help="skip timing the weight-absorption BMMs around the attention")
     ap.add_argument("--cpu-budget", type=float, default=15.0,

@@ -10,7 +10,9 @@ kernels); this package is its Python face:
   * `decode_step_host`, the same call for host-resident inputs (copies in,
     runs, copies the outputs back);
   * `absorb_q` / `absorb_o`, the weight-absorption BMMs on either side of
-    the attention (query through W_UK, output through W_UV).
+    the attention (query through W_UK, output through W_UV);
+  * `indexer_scores` / `topk_indices`, the sparse-attention indexer that
+    produces the top-k lists the sparse decode consumes.
 
 PyTorch is used only to allocate device memory and to name streams.
 """
@@ -37,6 +39,8 @@ from ._binding import (  # noqa: F401
     load,
     mla_absorb_o,
     mla_absorb_q,
+    mla_indexer_scores,
+    mla_topk,
     mla_combine,
     mla_decode,
     mla_decode_noalloc,
@@ -196,4 +200,49 @@ def absorb_o(o, w_uv, *, out=None, status=None, stream=None):
     if stream is None:
         stream = torch.cuda.current_stream(o.device)
     mla_absorb_o(o, o_stride, w_uv, T, H, out, out_stride, status, stream)
+    return out
+
+
+def indexer_scores(q_idx, w_idx, k_idx_cache, block_table, cache_lens, *, causal: bool = False,
+                   max_len: int | None = None, scores=None, status=None, stream=None):
+    """Index scores of every visible position.
+
+    q_idx [B, s_q, 64, 128] bf16, w_idx [B, s_q, 64] fp32, k_idx_cache
+    [num_pages, 64, 128] bf16 (paged like the latent cache, same block
+    table).  Returns `scores` (default a new fp32 [B, s_q, max_len] tensor;
+    positions past a token's visible count are left unwritten).
+    """
+    import torch
+    B, s_q = q_idx.shape[0], q_idx.shape[1]
+    if max_len is None:
+        max_len = block_table.shape[1] * PAGE
+    if scores is None:
+        stride = (max_len + 3) // 4 * 4
+        scores = torch.empty((B, s_q, stride), dtype=torch.float32, device=q_idx.device)
+    if status is None:
+        status = torch.zeros(1, dtype=torch.int32, device=q_idx.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q_idx.device)
+    mla_indexer_scores(q_idx, w_idx, k_idx_cache, k_idx_cache.shape[0], block_table, block_table.stride(0),
+                       cache_lens, B, s_q, MLA_FLAG_CAUSAL if causal else 0, max_len, scores, scores.stride(1),
+                       status, stream)
+    return scores
+
+
+def topk_indices(scores, cache_lens, topk: int, *, causal: bool = False, max_len: int | None = None, out=None,
+                 status=None, stream=None):
+    """Top-k lists [B, s_q, topk] int32 (increasing positions, -1 padded)
+    from index scores [B, s_q, stride] (as `indexer_scores` returns them)."""
+    import torch
+    B, s_q = scores.shape[0], scores.shape[1]
+    if max_len is None:
+        max_len = scores.shape[2]
+    if out is None:
+        out = torch.empty((B, s_q, topk), dtype=torch.int32, device=scores.device)
+    if status is None:
+        status = torch.zeros(1, dtype=torch.int32, device=scores.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(scores.device)
+    mla_topk(scores, scores.stride(1), cache_lens, B, s_q, MLA_FLAG_CAUSAL if causal else 0, max_len, topk, out,
+             status, stream)
     return out

@@ -30,7 +30,7 @@ MLA_FLAG_OUT_FP32 = 2
 MLA_FLAG_VALIDATE = 4
 MLA_FLAG_BF16_PV = 8
 
-# every symbol include/mla_decode.h and include/mla_absorb.h declare: name -> (restype, argtypes)
+# every symbol the headers in include/ declare: name -> (restype, argtypes)
 _c_int, _c_size, _vp, _i64, _f32, _uint = (ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p,
                                            ctypes.c_int64, ctypes.c_float, ctypes.c_uint)
 SIGNATURES = {
@@ -50,6 +50,9 @@ SIGNATURES = {
     "mla_status_string": (ctypes.c_char_p, [_c_int]),
     "mla_absorb_q": (_c_int, [_vp, _vp, _i64, _vp, _c_int, _c_int, _vp, _i64, _vp, _vp]),
     "mla_absorb_o": (_c_int, [_vp, _i64, _vp, _c_int, _c_int, _vp, _i64, _vp, _vp]),
+    "mla_indexer_scores": (_c_int, [_vp, _vp, _vp, _i64, _vp, _i64, _vp, _c_int, _c_int, _uint, _c_int, _vp, _i64,
+                                    _vp, _vp]),
+    "mla_topk": (_c_int, [_vp, _i64, _vp, _c_int, _c_int, _uint, _c_int, _c_int, _vp, _vp, _vp]),
 }
 
 _lib = None
@@ -200,3 +203,19 @@ def mla_absorb_o(o, o_stride: int, w_uv, num_tokens: int, num_heads: int, out, o
     _check("mla_absorb_o", load().mla_absorb_o(
         _ptr(o), int(o_stride), _ptr(w_uv), int(num_tokens), int(num_heads), _ptr(out), int(out_stride),
         _ptr(status), _stream(stream)))
+
+
+def mla_indexer_scores(q_idx, w_idx, k_idx_cache, num_pages: int, block_table, bt_stride: int, cache_lens,
+                       batch: int, s_q: int, flags: int, max_len: int, scores, scores_stride: int, status,
+                       stream=None) -> None:
+    _check("mla_indexer_scores", load().mla_indexer_scores(
+        _ptr(q_idx), _ptr(w_idx), _ptr(k_idx_cache), int(num_pages), _ptr(block_table), int(bt_stride),
+        _ptr(cache_lens), int(batch), int(s_q), int(flags), int(max_len), _ptr(scores), int(scores_stride),
+        _ptr(status), _stream(stream)))
+
+
+def mla_topk(scores, scores_stride: int, cache_lens, batch: int, s_q: int, flags: int, max_len: int, topk: int,
+             out_idx, status, stream=None) -> None:
+    _check("mla_topk", load().mla_topk(
+        _ptr(scores), int(scores_stride), _ptr(cache_lens), int(batch), int(s_q), int(flags), int(max_len),
+        int(topk), _ptr(out_idx), _ptr(status), _stream(stream)))

@@ -81,3 +81,23 @@ def absorb_q_bytes(num_tokens: int, with_pe: bool = True) -> int:
 def absorb_o_bytes(num_tokens: int) -> int:
     """O in, W_UV, O' out."""
     return num_tokens * H * D_V * 2 + H * D_V * D_NOPE * 2 + num_tokens * H * D_NOPE * 2
+
+
+# Sparse-attention indexer ("The 31-Millisecond Smoking Gun", DSA indexer):
+# per visible (query token, position) one 64-head x 128-dim product with the
+# index key, ReLU, a weighted head sum.  Bytes: every visible index key (256 B)
+# read once per query token, the 64 x 128 bf16 index query and 64 fp32 head
+# weights per query token, and the int32 list written; the fp32 scores that
+# pass between the two kernels are an intermediate and not counted.
+IDX_HEADS, IDX_DIM = 64, 128
+
+
+def indexer_flops(cache_lens, s_q: int, causal: bool) -> int:
+    n = int(visible_counts(cache_lens, s_q, causal).sum())
+    return n * (2 * IDX_HEADS * IDX_DIM + 3 * IDX_HEADS)
+
+
+def indexer_bytes(cache_lens, s_q: int, causal: bool, topk: int) -> int:
+    n = int(visible_counts(cache_lens, s_q, causal).sum())
+    B = np.asarray(cache_lens).size
+    return n * IDX_DIM * 2 + B * s_q * (IDX_HEADS * IDX_DIM * 2 + IDX_HEADS * 4 + topk * 4)

@@ -18,7 +18,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libmla_decode.so")
-SOURCES = ["decode_kernel.cu", "mtp_kernel.cu", "aux_kernels.cu", "api.cu", "noalloc.cu", "absorb_kernel.cu"]
+SOURCES = ["decode_kernel.cu", "mtp_kernel.cu", "aux_kernels.cu", "api.cu", "noalloc.cu", "absorb_kernel.cu",
+           "indexer_kernel.cu"]
 HEADERS = ["common.cuh", "kernel_common.cuh", "plan.cuh", "ptx.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -41,6 +42,7 @@ def _stale() -> bool:
     t = os.path.getmtime(LIB)
     deps = [os.path.join(CSRC, f) for f in SOURCES + HEADERS] + [
         os.path.join(ROOT, "include", "mla_decode.h"), os.path.join(ROOT, "include", "mla_absorb.h"),
+        os.path.join(ROOT, "include", "mla_indexer.h"),
         os.path.abspath(__file__)]
     return any(os.path.getmtime(d) > t for d in deps)
 

@@ -108,6 +108,21 @@ def test_absorption_calls_check_their_arguments_on_the_host(lib):
     assert lib.mla_absorb_q(*a) in (m.MLA_OK, m.MLA_ERR_DEVICE)
 
 
+def test_indexer_calls_check_their_arguments_on_the_host(lib):
+    ok = 1 << 20
+    sc = [ok, ok, ok, 10, ok, 4, ok, 2, 1, 0, 256, ok, 256, ok, None]
+    for i, v in [(0, None), (1, None), (2, None), (4, None), (6, None), (11, None), (13, None), (0, ok + 8),
+                 (3, 0), (5, 0), (7, 0), (9, 8), (10, 257), (12, 255), (12, 254), (13, ok + 2)]:
+        a = list(sc); a[i] = v
+        assert lib.mla_indexer_scores(*a) == m.MLA_ERR_INVALID_ARG, (i, v)
+    a = list(sc); a[8] = 9
+    assert lib.mla_indexer_scores(*a) == m.MLA_ERR_UNSUPPORTED
+    tk = [ok, 256, ok, 2, 1, 0, 256, 64, ok, ok, None]
+    for i, v in [(0, None), (2, None), (8, None), (9, None), (7, 0), (7, 65537), (1, 100), (8, ok + 2)]:
+        a = list(tk); a[i] = v
+        assert lib.mla_topk(*a) == m.MLA_ERR_INVALID_ARG, (i, v)
+
+
 def test_python_binding_raises_when_library_missing(tmp_path):
     from mla_latent_kv_09_gb300 import _binding
     saved = _binding._lib

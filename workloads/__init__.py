@@ -235,3 +235,29 @@ def make_absorb(num_tokens: int, num_heads: int = H, seed: int = 0, device="cpu"
     w_uk = _randn_bf16((num_heads, D_V, D_NOPE), seed, 22, device, scale=1.0 / math.sqrt(D_NOPE))
     w_uv = _randn_bf16((num_heads, D_V, D_NOPE), seed, 23, device, scale=1.0 / math.sqrt(D_V))
     return AbsorbInputs(q_proj=q, o=o, w_uk=w_uk, w_uv=w_uv)
+
+
+# ---------------------------------------------------------------- sparse-attention indexer
+H_IDX, D_IDX = 64, 128
+
+
+@dataclasses.dataclass
+class IndexerInputs:
+    q_idx: torch.Tensor    # bf16 [B, s_q, 64, 128]
+    w_idx: torch.Tensor    # fp32 [B, s_q, 64]
+    k_cache: torch.Tensor  # bf16 [num_pages, 64, 128]: index keys, same pages as the latent pool
+
+
+def make_indexer(w: Workload, seed: int = 0) -> IndexerInputs:
+    """Indexer inputs for a decode workload: one 128-dim index key per cached
+    token in the workload's pages (same block table), index queries of 64
+    heads per query token, head weights N(0, 1/64).  Keys and queries N(0,1)
+    in bf16."""
+    dev = w.q.device
+    B, s_q = w.batch, w.s_q
+    q = _randn_bf16((B, s_q, H_IDX, D_IDX), seed, 30, dev)
+    k = _randn_bf16((w.num_pages, PAGE, D_IDX), seed, 31, dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed * 1000003 + 32)
+    wt = torch.randn((B, s_q, H_IDX), generator=g, device=dev, dtype=torch.float32) / 8.0
+    return IndexerInputs(q_idx=q, w_idx=wt, k_cache=k)
