@@ -59,6 +59,7 @@ int mla_indexer_scores(const void* q_idx, const float* w_idx, const void* k_idx_
 /* Top-k of each (b, t) score row over its visible positions.
  *   scores, scores_stride, cache_lens, batch, s_q, flags, max_len: as above
  *   topk         1 .. 65536
+ *   max_len      at most 2,064,384 (MLA_ERR_UNSUPPORTED beyond)
  *   out_idx      int32 [batch, s_q, topk]: increasing positions, then -1
  */
 int mla_topk(const float* scores, int64_t scores_stride, const int32_t* cache_lens, int batch, int s_q,

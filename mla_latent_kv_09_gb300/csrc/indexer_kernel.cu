@@ -14,10 +14,12 @@
 //     (one position per thread) apply ReLU, weight and sum the 64 heads in
 //     fp32 and store the score.  HBM-bound: 256 B of keys per position.
 //   mla_topk_kernel: CTA = query token, 1024 threads.  Scores map to
-//     order-preserving 32-bit keys; three histogram passes (11, 11, 10 bits)
-//     find the k-th largest key T and how many keys equal to T to keep; a
-//     final ordered pass keeps every key > T and the first of those == T
-//     (smaller positions) and writes them in position order (block scans).
+//     order-preserving 32-bit keys; three histogram passes (11, 11, 10 bits;
+//     per-warp histograms: keys of similar magnitude share their top bits and
+//     would serialise on a few shared words) find the k-th largest key T and
+//     how many keys equal to T to keep; a final ordered pass keeps every key
+//     > T and the first of those == T (smaller positions) and writes them in
+//     position order (one block scan per 32 positions per thread).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -221,6 +223,28 @@ mla_indexer_scores_kernel(const __grid_constant__ IndexerParams p, const __grid_
 
 // ------------------------------------------------------------------ top-k
 constexpr int kKThreads = 1024;
+constexpr int kPer = 32;  // consecutive positions per thread and pass: 128 B of loads in flight
+constexpr int kKSmem = 32 * 1024 * 4;  // per-warp histograms
+// a warp counts at most kPer * 32 keys per span of kPer * kKThreads positions
+constexpr int kMaxTopkLen = (65535 / (kPer * 32)) * kPer * kKThreads;  // 2,064,384 positions per row
+
+// Scores j0 .. j0 + kPer - 1 of a row (0 past `vis`); the row's stride is a
+// multiple of 4 floats, so whole runs load as four 16-byte loads.
+__device__ __forceinline__ void load_run(const float* __restrict__ row, int j0, int vis, float (&v)[kPer]) {
+  if (j0 + kPer <= vis) {
+#pragma unroll
+    for (int i = 0; i < kPer / 4; ++i) {
+      const float4 f = __ldg(reinterpret_cast<const float4*>(row + j0) + i);
+      v[4 * i] = f.x;
+      v[4 * i + 1] = f.y;
+      v[4 * i + 2] = f.z;
+      v[4 * i + 3] = f.w;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) v[i] = j0 + i < vis ? __ldg(row + j0 + i) : 0.f;
+  }
+}
 
 // Order-preserving key of a finite float (larger float -> larger key; the
 // two zeros are one key).
@@ -260,6 +284,11 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int* 
 __global__ void __launch_bounds__(kKThreads)
 mla_topk_kernel(const float* __restrict__ scores, long long stride, const int* __restrict__ lens, int s_q,
                 int causal, int max_len, int topk, int* __restrict__ out) {
+  // per-warp histograms, two 16-bit bins per word (a warp counts at most
+  // kPer * 32 keys per span of kPer * 1024 positions, <= 65,535 for the
+  // kMaxTopkLen positions the host admits, so the halves never carry);
+  // merged into hist[] after each pass
+  extern __shared__ uint32_t warp_hist[];  // [32][1024]
   __shared__ int hist[2048];
   __shared__ int warp_sums[32];
   __shared__ int s_digit, s_above;
@@ -281,11 +310,27 @@ mla_topk_kernel(const float* __restrict__ scores, long long stride, const int* _
   for (int pass = 0; pass < 3; ++pass) {
     const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
     const int nb = pass == 2 ? 1024 : 2048;
-    for (int i = tid; i < nb; i += kKThreads) hist[i] = 0;
+    for (int i = tid; i < 32 * 1024; i += kKThreads) warp_hist[i] = 0u;
     __syncthreads();
-    for (int j = tid; j < vis; j += kKThreads) {
-      const uint32_t key = order_key(__ldg(row + j));
-      if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & (nb - 1)], 1);
+    uint32_t* wh = warp_hist + (tid >> 5) * 1024;
+    for (int base = 0; base < vis; base += kPer * kKThreads) {
+      const int j0 = base + tid * kPer;
+      float v[kPer];
+      load_run(row, j0, vis, v);
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        const uint32_t key = order_key(v[i]);
+        const bool in = j0 + i < vis && (key & mask) == prefix;
+        const uint32_t bin = in ? (key >> shift) & static_cast<uint32_t>(nb - 1) : 0xffffffffu;
+        if (in) atomicAdd(&wh[bin >> 1], 1u << (16u * (bin & 1u)));
+      }
+    }
+    __syncthreads();
+    for (int bin = tid; bin < nb; bin += kKThreads) {
+      int c = 0;
+#pragma unroll 8
+      for (int w = 0; w < 32; ++w) c += static_cast<int>((warp_hist[w * 1024 + (bin >> 1)] >> (16 * (bin & 1))) & 0xffffu);
+      hist[bin] = c;
     }
     __syncthreads();
     // bins from the top: thread i holds bins nb-1-per*i .. (descending)
@@ -314,20 +359,43 @@ mla_topk_kernel(const float* __restrict__ scores, long long stride, const int* _
   }
   const uint32_t T = prefix;  // keys > T are all taken, and the first krem keys == T
 
-  // ---- ordered output: positions ascending
+  // ---- ordered output, positions ascending: each thread owns kPer
+  // consecutive positions of a block-wide span; one scan of the per-thread
+  // counts places them
   int taken = 0, eq_seen = 0;
 #pragma unroll 1
-  for (int base = 0; base < vis; base += kKThreads) {
-    const int j = base + tid;
-    const uint32_t key = j < vis ? order_key(__ldg(row + j)) : 0u;
-    const bool gt = j < vis && key > T;
-    const bool eq = j < vis && key == T;
+  for (int base = 0; base < vis; base += kPer * kKThreads) {
+    const int j0 = base + tid * kPer;
+    uint32_t gt = 0, eq = 0;  // bit i: position j0 + i
+    float v[kPer];
+    load_run(row, j0, vis, v);
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      if (j0 + i < vis) {
+        const uint32_t key = order_key(v[i]);
+        gt |= static_cast<uint32_t>(key > T) << i;
+        eq |= static_cast<uint32_t>(key == T) << i;
+      }
+    }
     int eq_total = 0;
-    const int eq_rank = eq_seen + block_exclusive_scan(eq ? 1 : 0, warp_sums, &eq_total);
-    const bool sel = gt || (eq && eq_rank < krem);
+    int eq_rank = eq_seen + block_exclusive_scan(__popc(eq), warp_sums, &eq_total);
+    uint32_t sel = gt;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      if ((eq >> i) & 1u) {
+        if (eq_rank < krem) sel |= 1u << i;
+        ++eq_rank;
+      }
+    }
     int sel_total = 0;
-    const int at = taken + block_exclusive_scan(sel ? 1 : 0, warp_sums, &sel_total);
-    if (sel && at < topk) o[at] = j;
+    int at = taken + block_exclusive_scan(__popc(sel), warp_sums, &sel_total);
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      if ((sel >> i) & 1u) {
+        if (at < topk) o[at] = j0 + i;
+        ++at;
+      }
+    }
     taken += sel_total;
     eq_seen += eq_total;
   }
@@ -386,7 +454,8 @@ int indexer_device_ready() {
       return;
     }
     if (cudaFuncSetAttribute(mla_indexer_scores_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kISmem) !=
-        cudaSuccess) {
+            cudaSuccess ||
+        cudaFuncSetAttribute(mla_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kKSmem) != cudaSuccess) {
       cudaGetLastError();
       st.status = MLA_ERR_CUDA;
     }
@@ -452,8 +521,9 @@ int mla_topk(const float* scores, int64_t scores_stride, const int32_t* cache_le
   int rc = common_checks(cache_lens, batch, s_q, flags, max_len, scores, scores_stride, status);
   if (rc != MLA_OK) return rc;
   if (!out_idx || !al(out_idx, 4) || topk < 1 || topk > 65536) return MLA_ERR_INVALID_ARG;
+  if (max_len > kMaxTopkLen) return MLA_ERR_UNSUPPORTED;
   if ((rc = indexer_device_ready()) != MLA_OK) return rc;
-  mla_topk_kernel<<<batch * s_q, kKThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+  mla_topk_kernel<<<batch * s_q, kKThreads, kKSmem, static_cast<cudaStream_t>(stream)>>>(
       scores, scores_stride, cache_lens, s_q, (flags & MLA_FLAG_CAUSAL) ? 1 : 0, max_len, topk, out_idx);
   return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
