@@ -364,6 +364,23 @@ def roofline_of(w, r, pk, pk_kind, step_ms):
 
 
 ABSORB_SOURCES = ["absorb_kernel.cu", "kernel_common.cuh", "common.cuh", "ptx.cuh"]
+INDEXER_SOURCES = ["indexer_kernel.cu", "kernel_common.cuh", "common.cuh", "ptx.cuh"]
+
+
+def indexer_traffic():
+    """DRAM bytes per launch of the indexer scores kernel at the sparse
+    workload's size, from the committed (scaled) ncu record, if it was taken
+    on the current source (else None)."""
+    path = os.path.join(ROOT, "profiles", "indexer_traffic.json")
+    if not os.path.exists(path):
+        return None
+    h = hashlib.sha256()
+    for f in INDEXER_SOURCES:
+        h.update(open(os.path.join(ROOT, "mla_latent_kv_09_gb300", "csrc", f), "rb").read())
+    e = json.load(open(path)).get("mla_indexer_scores_kernel/sparse_b80")
+    if not e or e.get("kernel_hash") != h.hexdigest()[:16]:
+        return None
+    return e.get("dram_bytes_per_launch")
 
 
 def absorb_hash() -> str:
@@ -508,7 +525,8 @@ def time_indexer(m, args, dev, pk, pk_kind, with_cpu: bool):
            "us_scores": us_s, "us_topk": us_k, "us_per_call": us_g,
            "algorithmic_mb": nbytes / 1e6, "gflop": acc.indexer_flops(lens, s_q, False) / 1e9,
            "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                        "frac": gbs / pk["hbm_gbs"], "traffic": None, "kernel": "mla_indexer_scores_kernel",
+                        "frac": gbs / pk["hbm_gbs"], "traffic": indexer_traffic(),
+                        "kernel": "mla_indexer_scores_kernel",
                         "scope": "scores kernel alone: index-key bytes / its event time",
                         "peak_source": f"{pk_kind} (burst)"},
            "frac_roofline_call": nbytes / (pk["hbm_gbs"] * 1e9) / (us_g * 1e-6),
