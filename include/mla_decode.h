@@ -28,7 +28,8 @@
  * Three calls make one decode step, all asynchronous on `stream`:
  *     mla_decode_plan  -> partitions the (request, 64-token tile) work
  *     mla_decode       -> attention; writes final O/LSE for unsplit requests
- *                         and fp32 partials for split ones
+ *                         and 16-bit partials (fp16; bf16 with
+ *                         MLA_FLAG_BF16_PV) plus fp32 LSEs for split ones
  *     mla_combine      -> merges the partials, writes O/LSE of split requests
  *                         and of requests with nothing to attend to
  *
@@ -91,7 +92,9 @@ enum {
                             the O error grows to a few times 2e-2.  Every
                             other path, and this one by default, computes the
                             value product in fp16: value dims must then stay
-                            below 65504 in magnitude                        */
+                            below 65504 in magnitude.  On every path the flag
+                            also stores split requests' partial rows in bf16
+                            instead of fp16 (as wide in range as the values) */
 };
 
 enum { MLA_NUM_HEADS = 128, MLA_D_QK = 576, MLA_D_V = 512, MLA_PAGE = 64, MLA_MAX_SQ = 8 };
@@ -196,7 +199,8 @@ int mla_decode(const void* q, const void* kv_cache, int64_t num_pages,
 /*
  * Merge the split requests' partials (LSE = ln sum_s exp(lse_s),
  * O = sum_s exp(lse_s - LSE) * O_s) and write O = 0, LSE = -inf for
- * requests with nothing to attend to.  flags: MLA_FLAG_OUT_FP32 as above.
+ * requests with nothing to attend to.  flags: MLA_FLAG_OUT_FP32 as above,
+ * and MLA_FLAG_BF16_PV as given to mla_decode (it sets the partials' format).
  */
 int mla_combine(void* workspace, size_t ws_bytes, int batch, int s_q,
                 int num_heads, unsigned flags, int num_units, void* out,

@@ -18,7 +18,8 @@ __global__ void mla_plan_kernel(const int* lens, int B, int topk, int tile_rows,
                                 int* unit_meta, int* req_meta, int slots_cap);
 __global__ void mla_wait_timeout_kernel(int* status);
 __global__ void mla_combine_kernel(const int* hdr, const int* req_meta, const float* part_lse,
-                                   const float* part_o, int s_q, int out_fp32, void* out, float* lse);
+                                   const uint16_t* part_o, int part_bf16, int s_q, int out_fp32, void* out,
+                                   float* lse);
 __global__ void mla_validate_kernel(const int* lens, const int* bt, long long bt_stride,
                                     long long num_pages, int B, int s_q, const int* topk_idx, int topk,
                                     const uint16_t* kv, int check_range, int* status);
@@ -328,7 +329,8 @@ int mla_decode(const void* q, const void* kv_cache, int64_t num_pages, const int
   p.unit_meta = reinterpret_cast<const int*>(ws + L.units);
   p.req_meta = reinterpret_cast<const int*>(ws + L.reqs);
   p.part_lse = reinterpret_cast<float*>(ws + L.part_lse);
-  p.part_o = reinterpret_cast<float*>(ws + L.part_o);
+  p.part_o = reinterpret_cast<uint16_t*>(ws + L.part_o);
+  p.part_bf16 = (flags & MLA_FLAG_BF16_PV) ? 1 : 0;
 
   // the two-token kernel moves Q through its 8 KiB chunk slots: 64-row boxes
   CUtensorMap tm_q, tm_kv;
@@ -345,10 +347,10 @@ int mla_decode(const void* q, const void* kv_cache, int64_t num_pages, const int
     const uint64_t rows = static_cast<uint64_t>(num_pages) * kPage;
     if ((rc = encode_kv_3d(&tm_k3, kv_cache, rows, 3)) != MLA_OK) return rc;
     if ((rc = encode_kv_3d(&tm_v2, kv_cache, rows, 2)) != MLA_OK) return rc;
-    CUtensorMap tm_out, tm_part;  // O (bf16 or fp32) and the fp32 partials, for the epilogue's tensor stores
+    CUtensorMap tm_out, tm_part;  // O (bf16 or fp32) and the 16-bit partials, for the epilogue's tensor stores
     if ((rc = encode_out_2d(&tm_out, out, static_cast<uint64_t>(batch) * s_q * kHeads, p.out_fp32 != 0)) != MLA_OK)
       return rc;
-    if ((rc = encode_out_2d(&tm_part, p.part_o, static_cast<uint64_t>(L.slots) * s_q * kHeads, true)) != MLA_OK)
+    if ((rc = encode_out_2d(&tm_part, p.part_o, static_cast<uint64_t>(L.slots) * s_q * kHeads, false)) != MLA_OK)
       return rc;
     e = mtp_launch((flags & MLA_FLAG_BF16_PV) != 0, U, s, p, tm_q, tm_k3, tm_v2, tm_out, tm_part);
   } else {
@@ -390,8 +392,9 @@ int mla_combine(void* workspace, size_t ws_bytes, int batch, int s_q, int num_he
   const cudaError_t e =
       cudaLaunchKernelEx(&cfg, mla_combine_kernel, reinterpret_cast<const int*>(ws + L.hdr),
                          reinterpret_cast<const int*>(ws + L.reqs),
-                         reinterpret_cast<const float*>(ws + L.part_lse), reinterpret_cast<const float*>(ws + L.part_o),
-                         s_q, (flags & MLA_FLAG_OUT_FP32) ? 1 : 0, out, lse);
+                         reinterpret_cast<const float*>(ws + L.part_lse),
+                         reinterpret_cast<const uint16_t*>(ws + L.part_o), (flags & MLA_FLAG_BF16_PV) ? 1 : 0, s_q,
+                         (flags & MLA_FLAG_OUT_FP32) ? 1 : 0, out, lse);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return MLA_ERR_CUDA;

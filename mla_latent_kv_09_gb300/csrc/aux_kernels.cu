@@ -1,5 +1,6 @@
 // aux_kernels.cu — the split-KV planner, the LSE combine and the input
 // validator of the MLA decode library (sm_103a).
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -113,8 +114,8 @@ __global__ void __launch_bounds__(1024) mla_plan_kernel(const int* __restrict__ 
 __global__ void __launch_bounds__(256) mla_combine_kernel(const int* __restrict__ hdr,
                                                           const int* __restrict__ req_meta,
                                                           const float* __restrict__ part_lse,
-                                                          const float* __restrict__ part_o, int s_q,
-                                                          int out_fp32, void* out, float* lse) {
+                                                          const uint16_t* __restrict__ part_o, int part_bf16,
+                                                          int s_q, int out_fp32, void* out, float* lse) {
   grid_launch_dependents();  // a kernel launched after this one may set up (it waits for this grid)
   grid_dependency_wait();    // the decode kernel has finished (programmatic dependent launch)
   if (hdr[kHdrStatus] != 0) return;  // a failed check or wait: the step's outputs stay unwritten
@@ -147,8 +148,22 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(const int* __restrict_
       for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
       LSE = m + logf(sum);
       const float w_l = lane < ns ? expf(lse_l - LSE) : 0.f;
+      // partial rows are 16-bit (fp16, or bf16 with MLA_FLAG_BF16_PV): lane
+      // reads dims {4*lane + 128*k .. +3} as one 8-byte piece per k
       auto row = [&](int s) {
-        return reinterpret_cast<const float4*>(part_o + ((static_cast<long long>(slot0 + s) * s_q + t) * kHeads + h) * kDv) + lane;
+        return reinterpret_cast<const uint2*>(part_o + ((static_cast<long long>(slot0 + s) * s_q + t) * kHeads + h) * kDv) + lane;
+      };
+      auto widen = [&](uint2 u) {
+        float4 f;
+        if (part_bf16) {
+          f.x = __uint_as_float(u.x << 16); f.y = __uint_as_float(u.x & 0xffff0000u);
+          f.z = __uint_as_float(u.y << 16); f.w = __uint_as_float(u.y & 0xffff0000u);
+        } else {
+          const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+          const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+          f = make_float4(a.x, a.y, b.x, b.y);
+        }
+        return f;
       };
       auto add = [&](float w, const float4 (&v)[4]) {
         if (w == 0.f) return;  // an empty split adds nothing
@@ -161,23 +176,29 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(const int* __restrict_
       const int n32 = ns < 32 ? ns : 32;
       int s = 0;
       for (; s + 2 <= n32; s += 2) {
-        const float4* r0 = row(s);
-        const float4* r1 = row(s + 1);
+        const uint2* r0 = row(s);
+        const uint2* r1 = row(s + 1);
+        uint2 u0[4], u1[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          u0[k] = r0[32 * k];
+          u1[k] = r1[32 * k];
+        }
         float4 v0[4], v1[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          v0[k] = r0[32 * k];
-          v1[k] = r1[32 * k];
+          v0[k] = widen(u0[k]);
+          v1[k] = widen(u1[k]);
         }
         add(__shfl_sync(0xffffffffu, w_l, s), v0);
         add(__shfl_sync(0xffffffffu, w_l, s + 1), v1);
       }
       for (; s < ns; ++s) {  // the odd split, and splits past 32
         const float w = s < 32 ? __shfl_sync(0xffffffffu, w_l, s) : expf(lse_of(s) - LSE);
-        const float4* r0 = row(s);
+        const uint2* r0 = row(s);
         float4 v0[4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) v0[k] = r0[32 * k];
+        for (int k = 0; k < 4; ++k) v0[k] = widen(r0[32 * k]);
         add(w, v0);
       }
     }

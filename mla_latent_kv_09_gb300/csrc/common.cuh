@@ -33,7 +33,7 @@ __host__ __device__ inline WsLayout ws_layout(int batch, int s_q, int num_units)
   L.units = off;    off += align256(static_cast<size_t>(num_units) * 5 * sizeof(int));
   L.reqs = off;     off += align256(static_cast<size_t>(batch) * 4 * sizeof(int));
   L.part_lse = off; off += align256(static_cast<size_t>(L.slots) * s_q * kHeads * sizeof(float));
-  L.part_o = off;   off += align256(static_cast<size_t>(L.slots) * s_q * kHeads * kDv * sizeof(float));
+  L.part_o = off;   off += align256(static_cast<size_t>(L.slots) * s_q * kHeads * kDv * sizeof(uint16_t));
   L.total = off;
   return L;
 }
@@ -71,7 +71,8 @@ struct DecodeParams {
   const int* unit_meta;       // [U, 5]
   const int* req_meta;        // [B, 4]
   float* part_lse;            // [slots, s_q, 128]
-  float* part_o;              // [slots, s_q, 128, 512]
+  uint16_t* part_o;           // [slots, s_q, 128, 512], fp16 (bf16 when part_bf16)
+  int part_bf16;              // partial rows in bf16 (MLA_FLAG_BF16_PV) instead of fp16
 };
 
 }  // namespace mla

@@ -430,26 +430,38 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
           if (!(ok = warp_wait(bar(kOF), nseg & 1u, ctl))) break;
           tc_fence_after();
           const long long bt_row = static_cast<long long>(sg.b) * p.s_q + tok;
-          if (sg.slot < 0 && !p.out_fp32) {
-            uint16_t* dst0 = static_cast<uint16_t*>(p.out) + (bt_row * kHeads + row) * kDv;
+          // final bf16 O, or a 16-bit partial (fp16: O of a split is a convex
+          // combination of value rows, which the fp16 value product keeps
+          // below 65504; bf16 with MLA_FLAG_BF16_PV), or final fp32 O
+          const bool part = sg.slot >= 0;
+          if (part && sg.slot >= 2 * U) {
+            // the plan never uses more than 2 * (U - 1) slots
+          } else if (part || !p.out_fp32) {
+            uint16_t* dst0 = part
+                ? p.part_o + ((static_cast<long long>(sg.slot) * p.s_q + tok) * kHeads + row) * kDv
+                : static_cast<uint16_t*>(p.out) + (bt_row * kHeads + row) * kDv;
+            const bool f16 = part && !p.part_bf16;
 #pragma unroll 1
             for (int cc = 0; cc < 16; ++cc) {
               uint32_t r[32];
               tmem_ld32(tmem + lane_base + kColO + 32u * cc, r);
               tmem_wait_ld();
               uint4* dst = reinterpret_cast<uint4*>(dst0 + 32 * cc);
+              uint32_t w[16];
+              if (f16) {
 #pragma unroll
-              for (int k = 0; k < 4; ++k)
-                dst[k] = make_uint4(
-                    pack_bf16x2(__uint_as_float(r[8 * k + 0]) * fin, __uint_as_float(r[8 * k + 1]) * fin),
-                    pack_bf16x2(__uint_as_float(r[8 * k + 2]) * fin, __uint_as_float(r[8 * k + 3]) * fin),
-                    pack_bf16x2(__uint_as_float(r[8 * k + 4]) * fin, __uint_as_float(r[8 * k + 5]) * fin),
-                    pack_bf16x2(__uint_as_float(r[8 * k + 6]) * fin, __uint_as_float(r[8 * k + 7]) * fin));
+                for (int c = 0; c < 16; ++c)
+                  w[c] = pack_f16x2(__uint_as_float(r[2 * c]) * fin, __uint_as_float(r[2 * c + 1]) * fin);
+              } else {
+#pragma unroll
+                for (int c = 0; c < 16; ++c)
+                  w[c] = pack_bf16x2(__uint_as_float(r[2 * c]) * fin, __uint_as_float(r[2 * c + 1]) * fin);
+              }
+#pragma unroll
+              for (int k = 0; k < 4; ++k) dst[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
             }
-          } else if (sg.slot < 2 * U) {
-            float* dst0 = sg.slot < 0
-                ? static_cast<float*>(p.out) + (bt_row * kHeads + row) * kDv
-                : p.part_o + ((static_cast<long long>(sg.slot) * p.s_q + tok) * kHeads + row) * kDv;
+          } else {
+            float* dst0 = static_cast<float*>(p.out) + (bt_row * kHeads + row) * kDv;
 #pragma unroll 1
             for (int cc = 0; cc < 16; ++cc) {
               uint32_t r[32];

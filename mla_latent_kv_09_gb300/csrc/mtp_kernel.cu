@@ -409,7 +409,7 @@ mla_decode_mtp_kernel(const __grid_constant__ DecodeParams p, const __grid_const
   auto epilogue_share = [&](int w, float fin, const Seg& sg, uint32_t pb) {
     const bool to_part = sg.slot >= 0;
     if (to_part && sg.slot >= 2 * U) return;  // the plan never uses more than 2 * (U - 1) slots
-    const bool f32 = to_part || p.out_fp32;
+    const bool f32 = !to_part && p.out_fp32;  // partials are 16-bit (fp16, or bf16 with kBf16PV)
     const CUtensorMap* tm = to_part ? &tm_part : &tm_out;
     const long long orow = to_part ? static_cast<long long>(sg.slot) * 2 + tok : static_cast<long long>(sg.b) * 2 + tok;
     const int y = static_cast<int>(orow * kHeads) + 32 * (w & 3);
@@ -434,9 +434,15 @@ mla_decode_mtp_kernel(const __grid_constant__ DecodeParams p, const __grid_const
         uint32_t r[32];
         tmem_ld32(taddr + static_cast<uint32_t>(32 * i), r);
         tmem_wait_ld();
+        if (to_part && !kBf16PV) {
 #pragma unroll
-        for (int c = 0; c < 16; ++c)
-          v[c] = pack_bf16x2(__uint_as_float(r[2 * c]) * fin, __uint_as_float(r[2 * c + 1]) * fin);
+          for (int c = 0; c < 16; ++c)
+            v[c] = pack_f16x2(__uint_as_float(r[2 * c]) * fin, __uint_as_float(r[2 * c + 1]) * fin);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 16; ++c)
+            v[c] = pack_bf16x2(__uint_as_float(r[2 * c]) * fin, __uint_as_float(r[2 * c + 1]) * fin);
+        }
       }
       if (i > 0) {  // the previous box's store has read the staging
         if (lane == 0) bulk_wait_read();

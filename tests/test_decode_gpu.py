@@ -216,14 +216,16 @@ def test_two_token_peaked_softmax_default_mode_meets_the_bar():
 def test_two_token_peaked_softmax_bf16_mode_stays_within_its_stated_error():
     # MLA_FLAG_BF16_PV keeps 8 significant bits on the weights: on the same
     # peaked input its O error is a few times the bar (an fp64 emulation of
-    # the kernel's rounding gives max-abs 0.03-0.05, mean-abs ~1.3e-3); the
-    # LSE does not depend on the value precision and still meets its bar
+    # the kernel's rounding gives max-abs 0.03-0.05, mean-abs ~1.3e-3), and
+    # the partial rows of split requests are bf16 too (one more rounding of
+    # those rows, <= 2^-9 relative); the LSE does not depend on the value
+    # precision and still meets its bar
     w = wl.make_workload("mtp_spiked", [6000, 3000, 129], s_q=2, causal=True, spike_frac=0.05, seed=31,
                          device="cuda")
     o_ref, lse_ref = reference(w)
     o, lse = run(w, bf16_pv=True)
     err = np.abs(o - o_ref)
-    assert err.max() <= 0.1 and err.mean() <= 3e-3, (err.max(), err.mean())
+    assert err.max() <= 0.1 and err.mean() <= 4e-3, (err.max(), err.mean())
     fin = np.isfinite(lse_ref)
     assert np.abs(lse[fin] - lse_ref[fin]).max() <= LSE_MAX
 

@@ -139,12 +139,13 @@ def _align256(x):
 def ws_offsets(B, s_q, U):
     """Byte offsets of the workspace's unit table and request table, and its
     size: header (64 ints), unit table (U x 5 ints), request table (B x 4
-    ints), partial LSE and partial O (2U slots), each 256-byte aligned."""
+    ints), fp32 partial LSE and 16-bit partial O (2U slots), each 256-byte
+    aligned."""
     off_units = _align256(64 * 4)
     off_reqs = off_units + _align256(U * 5 * 4)
     slots = 2 * U
     total = (off_reqs + _align256(B * 4 * 4) + _align256(slots * s_q * 128 * 4)
-             + _align256(slots * s_q * 128 * 512 * 4))
+             + _align256(slots * s_q * 128 * 512 * 2))
     return off_units, off_reqs, total
 
 
