@@ -61,7 +61,8 @@ def _same(a, b):
 
 @pytest.mark.parametrize("name,kw", [("mtp_b64", dict(batch=16, length=3000)),
                                      ("uniform_b32", dict(batch=8, length=2000)),
-                                     ("sparse_b80", dict(batch=4, length=5000))])
+                                     ("sparse_b80", dict(batch=4, length=5000)),
+                                     ("mtp4_b64", dict(batch=12, length=2500))])
 def test_noalloc_matches_allocating_entry_point_twice(name, kw):
     w = wl.make_config(name, device="cuda", **kw)
     ref = _allocating(w, out_fp32=True)
