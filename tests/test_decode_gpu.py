@@ -260,6 +260,19 @@ def test_two_token_sparse_uses_per_token_lists():
     assert_close(o, lse, o_ref, lse_ref)
 
 
+def test_many_short_requests_beyond_the_plans_shared_table():
+    # 5,000 requests (the plan keeps at most 4,096 in shared memory and walks
+    # the rest through global memory), lengths 0..300 with empty ones;
+    # sampled requests against the oracle, empty ones O = 0, LSE = -inf
+    lens = np.random.default_rng(77).integers(0, 301, size=5000)
+    lens[::97] = 0
+    w = wl.make_workload("many", lens, seed=78, device="cuda")
+    o, lse = run(w)
+    sel = [(b, 0) for b in (0, 1, 97, 1234, 4095, 4096, 4097, 4999)]
+    o_ref, lse_ref = reference(w, select=sel)
+    assert_close(o, lse, o_ref, lse_ref, select=sel)
+
+
 # ---------------------------------------------------------------- more than two query tokens (s_q = 3 .. 8)
 
 @pytest.mark.parametrize("s_q", [3, 4, 8])
