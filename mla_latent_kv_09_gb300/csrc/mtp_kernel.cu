@@ -30,9 +30,12 @@
 //     rank 2 issues O += P V (M = 256, N = 2 x 256, K = 128).  At the end of
 //     a segment all sixteen warps write O (scaled by 1 / z) with tensor
 //     stores, staged in the P slot the last tile used.
-// P and V are bf16 (the kBf16PV variant, the default), or fp16 on request
-// (11 significant bits on the softmax weights instead of 8; values must then
-// stay below 65504 in magnitude, and V is converted in shared memory).
+// P and V are fp16 by default (11 significant bits on the softmax weights;
+// values must stay below 65504 in magnitude): the value ranks' conversion
+// warps read each page's value dims from global memory (an L2 hit behind the
+// score ranks' loads), convert them and store them into the page slot, each
+// warp announcing its rows to rank 2 itself.  The kBf16PV variant (bf16 P and
+// V, on request) loads the value dims with TMA instead.
 //
 // Warps (640 threads).  Score ranks: 0-15 softmax (warp w: head rows
 // 32 (w % 4) .., key columns 32 (w / 4) .. of each tile), 16 and 19 MMA issue
@@ -67,6 +70,15 @@
 
 namespace mla {
 namespace mtp {
+
+// Arrive on an mbarrier of the value pair's rank 2 with release at CTA scope:
+// the arriving warp's shared-memory stores are performed before the arrive
+// lands.  The tensor core of the pair reads them from this CTA's shared memory
+// only after rank 2 has seen the arrival.  (Release at cluster scope costs
+// each arriving warp about a thousand cycles under load.)
+__device__ __forceinline__ void mbar_arrive_remote_cta(uint32_t remote_bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cluster.b64 _, [%0];" ::"r"(remote_bar) : "memory");
+}
 
 constexpr int kTileRows = 2 * kPage;              // 128 cached rows per tile
 constexpr int kPageChunk = kPage * 128;           // 8 KiB: 64 rows x 64 dims (bf16), 128B-swizzled
@@ -247,7 +259,7 @@ mla_decode_mtp_kernel(const __grid_constant__ DecodeParams p, const __grid_const
     for (int i = 0; i < kVSlots; ++i) {
       mbar_init(bar(kVF + i), 1);
       mbar_init(bar(kVE + i), 1);
-      mbar_init(bar(kVR + i), 2);
+      mbar_init(bar(kVR + i), kBf16PV ? 2 : 2 * (kConvThreads / 32));  // fp16: every conversion warp of both
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(kSF + i), 1);
@@ -867,28 +879,8 @@ mla_decode_mtp_kernel(const __grid_constant__ DecodeParams p, const __grid_const
           }
         }
       }
+      // (fp16 variant: the conversion warps load the value dims themselves)
       Ring<kVSlots> rv;
-      if (!kBf16PV) {
-        // fp16 variant: the conversion warps load the value dims themselves;
-        // this warp announces each stored page to rank 2 (a release at
-        // cluster scope, cumulative over the group's writes it observed at
-        // named barrier 8) and votes with the group at barrier 7
-        const uint32_t rVR = mapa(bar(kVR), 2);
-        bool go = true;
-        while (go && it.next(sg)) {
-          for (int j = sg.t0; j < sg.t1 && go; ++j) {
-            for (int e = 0; e < 2; ++e, rv.advance()) {
-              const bool w_ok = warp_wait(bar(kVE + rv.idx), rv.phase ^ 1u, ctl);
-              if (!named_bar_all(7, kConvThreads + 32, w_ok)) {
-                go = false;
-                break;
-              }
-              named_bar_sync(8, kConvThreads + 32);
-              if (lane == 0) mbar_arrive_remote(rVR + 8u * rv.idx);
-            }
-          }
-        }
-      }
       while (kBf16PV && ok && it.next(sg)) {
         const int L = max(p.cache_lens[sg.b], 0);
         const int* bt_row = p.block_table + static_cast<long long>(sg.b) * p.bt_stride;
@@ -955,14 +947,31 @@ mla_decode_mtp_kernel(const __grid_constant__ DecodeParams p, const __grid_const
     // kVDepth pages of loads in flight per thread (registers), so that a
     // page's load latency spans several pages' turns
     uint4 v[kVDepth][kRowsPerThread];
-    // page pi of the current segment's request (pool page, or -1 past the
-    // cache end / outside the pool) into buffer d; rows >= L - 64 pi are zeros
-    auto load_page = [&](uint4 (&dst)[kRowsPerThread], const int* bt_row, int L, int pi) {
+    // Page ids of the segment, 32 at a time and one batch ahead: lane j holds
+    // the pool page of page ids_base + j (-1 past the cache end or outside the
+    // pool).  Reading the block-table entry next to each page's loads would
+    // put an L2 round trip (the entry does not stay in the small L1 that the
+    // value stream passes through) in front of every page.
+    const int* bt_row = nullptr;
+    int L = 0, ids_base = 0, ids_cur = -1, ids_next = -1;
+    auto fetch_ids = [&](int base) {
+      const int pi = base + lane;
       int page = -1;
       if (pi < (L + kPage - 1) / kPage && pi < p.bt_stride) {
         const int pg = __ldg(bt_row + pi);
         page = (pg >= 0 && pg < p.num_pages) ? pg : -1;
       }
+      return page;
+    };
+    // page pi of the current segment's request into buffer dst; rows >= L -
+    // 64 pi are zeros.  Called by whole warps with pi increasing by one.
+    auto load_page = [&](uint4 (&dst)[kRowsPerThread], int pi) {
+      if (pi >= ids_base + 32) {
+        ids_base += 32;
+        ids_cur = ids_next;
+        ids_next = fetch_ids(ids_base + 32);
+      }
+      const int page = __shfl_sync(0xffffffffu, ids_cur, pi - ids_base);
       const int rows = L - pi * kPage;
       const uint16_t* src = p.kv + static_cast<long long>(page >= 0 ? page : 0) * (kPage * kDqk) + gcol;
 #pragma unroll
@@ -971,53 +980,59 @@ mla_decode_mtp_kernel(const __grid_constant__ DecodeParams p, const __grid_const
         dst[i] = (page >= 0 && r < kPage && r < rows) ? ld_global_nc_v4(src + r * kDqk) : make_uint4(0u, 0u, 0u, 0u);
       }
     };
+    const uint32_t rVR = mapa(bar(kVR), 2);
     SegIter it(p, unit);
     Seg sg;
     Ring<kVSlots> rv;
     uint32_t g = 0, nseg = 0;
-    bool stop = false;  // the twelve warps vote at every named barrier
-    while (!stop && it.next(sg)) {
-      const int L = max(p.cache_lens[sg.b], 0);
-      const int* bt_row = p.block_table + static_cast<long long>(sg.b) * p.bt_stride;
+    // this warp's waits so far; the twelve warps vote at each segment's
+    // epilogue barrier, so a warp whose wait failed skips the rest of the
+    // segment's pages and they all leave there together
+    bool wok = true;
+    while (it.next(sg)) {
+      L = max(p.cache_lens[sg.b], 0);
+      bt_row = p.block_table + static_cast<long long>(sg.b) * p.bt_stride;
       const int p0 = 2 * sg.t0, np = 2 * (sg.t1 - sg.t0);  // this segment's pages: p0 .. p0 + np - 1
+      ids_base = p0;
+      ids_cur = fetch_ids(p0);
+      ids_next = fetch_ids(p0 + 32);
 #pragma unroll
       for (int d = 0; d < kVDepth; ++d)
-        if (d < np) load_page(v[d], bt_row, L, p0 + d);
-      for (int q0 = 0; q0 < np && !stop; q0 += kVDepth) {
+        if (wok && d < np) load_page(v[d], p0 + d);
+      for (int q0 = 0; q0 < np; q0 += kVDepth) {
 #pragma unroll
         for (int d = 0; d < kVDepth; ++d) {
           const int q = q0 + d;
           if (q >= np) break;
-          const bool ok = warp_wait(bar(kVE + rv.idx), rv.phase ^ 1u, ctl);  // PV is done with the slot
-          if (!named_bar_all(7, kConvThreads + 32, ok)) {  // with the announcing warp
-            stop = true;
-            break;
-          }
-          const uint32_t stg = vslot(rv.idx) + scol;
+          wok = wok && warp_wait(bar(kVE + rv.idx), rv.phase ^ 1u, ctl);  // PV is done with the slot
+          if (wok) {
+            const uint32_t stg = vslot(rv.idx) + scol;
 #pragma unroll
-          for (int i = 0; i < kRowsPerThread; ++i) {
-            const int r = lw + 12 * i;
-            if (r < kPage)
-              st_shared_v4(stg + static_cast<uint32_t>(r) * 128u + ((spc ^ static_cast<uint32_t>(r & 7)) << 4),
-                           bf16x2_to_f16x2(v[d][i].x), bf16x2_to_f16x2(v[d][i].y), bf16x2_to_f16x2(v[d][i].z),
-                           bf16x2_to_f16x2(v[d][i].w));
+            for (int i = 0; i < kRowsPerThread; ++i) {
+              const int r = lw + 12 * i;
+              if (r < kPage)
+                st_shared_v4(stg + static_cast<uint32_t>(r) * 128u + ((spc ^ static_cast<uint32_t>(r & 7)) << 4),
+                             bf16x2_to_f16x2(v[d][i].x), bf16x2_to_f16x2(v[d][i].y),
+                             bf16x2_to_f16x2(v[d][i].z), bf16x2_to_f16x2(v[d][i].w));
+            }
+            fence_proxy_async_smem();  // generic writes, read next by the tensor core
+            __syncwarp();
+            // Each warp announces its own rows to rank 2 (release, cumulative
+            // over the warp's stores), before its loads of the next page.  One
+            // announcer per rank after a group barrier put that barrier and
+            // the announcer's release on every page's path.
+            if (lane == 0) mbar_arrive_remote_cta(rVR + 8u * rv.idx);
           }
-          fence_proxy_async_smem();  // generic writes, read next by the tensor core
-          // the TMA warp, which has no loads in flight, announces the page: a
-          // release arrive from a thread of this group would first wait for
-          // its own prefetch loads of the next pages
-          named_bar_sync(8, kConvThreads + 32);
           rv.advance();
           // the segment's page kVDepth ahead goes into the buffer just stored
-          if (q + kVDepth < np) load_page(v[d], bt_row, L, p0 + q + kVDepth);
+          if (wok && q + kVDepth < np) load_page(v[d], p0 + q + kVDepth);
         }
       }
-      if (stop) break;
       g += static_cast<uint32_t>(sg.t1 - sg.t0);
       {  // ---- this group's share of the segment epilogue
         const uint32_t pb = (g - 1u) & 1u;  // the segment's last tile
         // O complete; the last P message (with the final scales) landed
-        bool ok = warp_wait(bar(kOF), nseg & 1u, ctl) && warp_wait(bar(kPM + pb), ((g - 1u) >> 1) & 1u, ctl);
+        bool ok = wok && warp_wait(bar(kOF), nseg & 1u, ctl) && warp_wait(bar(kPM + pb), ((g - 1u) >> 1) & 1u, ctl);
         if (!named_bar_all(6, kConvThreads, ok)) break;
         tc_fence_after();
         epilogue_share(warp, fin_s[pb * kHeads + 32 * (warp & 3) + lane], sg, pb);
@@ -1058,7 +1073,7 @@ mla_decode_mtp_kernel(const __grid_constant__ DecodeParams p, const __grid_const
           }
           fence_proxy_async_smem();
           named_bar_sync(6, kConvThreads);
-          if (ptid == 0) mbar_arrive_remote(rVR + 8u * rv.idx);
+          if (ptid == 0) mbar_arrive_remote_cta(rVR + 8u * rv.idx);
         }
         if (!stop && j == sg.t1 - 1) {  // ---- this group's share of the segment epilogue
           const uint32_t pb = g & 1u;
