@@ -1,6 +1,6 @@
-"""Plain fp64 CPU oracle for absorbed-MLA decode attention, the
-weight-absorption BMMs on either side of it, and the sparse-attention
-indexer (token scores, top-k lists).
+"""Plain fp64 CPU oracle for absorbed-MLA decode attention (over a bf16 or an
+FP8 latent cache), the weight-absorption BMMs on either side of it, and the
+sparse-attention indexer (token scores, top-k lists).
 
 TEST INFRASTRUCTURE ONLY.  Nothing in the product path (the CUDA library, its
 Python binding, the timed legs of the benchmark) may import or call this
@@ -23,3 +23,4 @@ from .mla_oracle import (  # noqa: F401
 )
 from .absorb_oracle import absorb_o, absorb_q  # noqa: F401,E402
 from .indexer_oracle import indexer_scores, indexer_topk, topk_select, topk_select_fast  # noqa: F401,E402
+from .fp8_oracle import e4m3_to_f64, fp8_rows_to_f64, mla_decode_fp8, ue8m0_to_f64  # noqa: F401,E402
