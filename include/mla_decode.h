@@ -94,8 +94,33 @@ enum {
                             value product in fp16: value dims must then stay
                             below 65504 in magnitude.  On every path the flag
                             also stores split requests' partial rows in bf16
-                            instead of fp16 (as wide in range as the values) */
+                            instead of fp16 (as wide in range as the values) */,
+  MLA_FLAG_KV_FP8 = 16   /* the cache is FP8 (see MLA_FP8_ROW_BYTES): the
+                            latent caching in FP8 of "The 31-Millisecond
+                            Smoking Gun" (DeepSeek-V4-Flash paragraph) and the
+                            precision lever of "How DeepSeek Inference Works".
+                            One-token kernel paths only: every s_q with top-k
+                            lists, and s_q != 2 dense (MLA_ERR_UNSUPPORTED
+                            for s_q = 2 dense).  mla_combine accepts the flag
+                            and ignores it. */
 };
+
+/*
+ * FP8 cache rows (MLA_FLAG_KV_FP8).  The pages give no byte format; the
+ * reading implemented is a 656-byte row per cached token:
+ *   bytes [0, 512)    the 512 latent dims as OCP FP8 E4M3 codes (bias 7, no
+ *                     infinities, S.1111.111 = NaN)
+ *   bytes [512, 516)  one UE8M0 scale per 128-dim group of the latent:
+ *                     scale = 2^(byte - 127)
+ *   bytes [516, 528)  unused
+ *   bytes [528, 656)  the 64 RoPE dims in bf16
+ * Latent dim d = e4m3(byte d) * scale[d / 128].  Power-of-two scales make
+ * every such value exact in bf16 (the score operand) and, below 65504 in
+ * magnitude, in fp16 (the value operand), so the step attends over exactly
+ * the values the rows encode.  A page is 64 rows (41,984 bytes); the block
+ * table is unchanged.
+ */
+enum { MLA_FP8_ROW_BYTES = 656 };
 
 enum { MLA_NUM_HEADS = 128, MLA_D_QK = 576, MLA_D_V = 512, MLA_PAGE = 64, MLA_MAX_SQ = 8 };
 
@@ -156,7 +181,8 @@ int mla_decode_plan_host(const int32_t* cache_lens_host, int batch, int s_q,
 /*
  * Attention for one decode step (after mla_decode_plan on the same stream).
  *   q            bf16 [batch, s_q, 128, 576], contiguous, 16-B aligned
- *   kv_cache     bf16 [num_pages, 64, 576], contiguous, 16-B aligned
+ *   kv_cache     bf16 [num_pages, 64, 576], contiguous, 16-B aligned; with
+ *                MLA_FLAG_KV_FP8 bytes [num_pages, 64, 656] (FP8 rows)
  *   num_pages    pages in the pool (rows = 64 * num_pages)
  *   block_table  int32, row b at block_table + b * bt_stride; entries
  *                0 .. ceil(len_b / 64) - 1 are read
@@ -182,7 +208,8 @@ int mla_decode_plan_host(const int32_t* cache_lens_host, int batch, int s_q,
  * MLA_ERR_BAD_TABLE, MLA_ERR_BAD_INDEX or (wherever the value product is
  * fp16, i.e. everywhere but the MLA_FLAG_BF16_PV two-token path)
  * MLA_ERR_VALUE_RANGE for a visible value dim that is not finite or has
- * |v| >= 65536; the attention and combine kernels then leave O and LSE
+ * |v| >= 65536 (FP8 rows: a NaN code, a scale byte of 255, or a scaled
+ * latent dim of 65536 or more); the attention and combine kernels then leave O and LSE
  * unwritten.  It reads every visible cache row once more (a full pass over
  * the cache: a debugging aid, not a production mode).  The call does not
  * synchronise: read the outcome with mla_workspace_status.

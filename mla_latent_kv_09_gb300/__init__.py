@@ -31,6 +31,7 @@ from ._binding import (  # noqa: F401
     MLA_ERR_WORKSPACE,
     MLA_FLAG_CAUSAL,
     MLA_FLAG_BF16_PV,
+    MLA_FLAG_KV_FP8,
     MLA_FLAG_OUT_FP32,
     MLA_FLAG_VALIDATE,
     MLA_OK,
@@ -77,7 +78,8 @@ def decode_step(q, kv_cache, block_table, cache_lens, softmax_scale: float, *, c
                 num_units: int = 0, workspace: Workspace | None = None, out=None, lse=None, stream=None):
     """One MLA decode step on device tensors: plan, attention, combine.
 
-    q [B, s_q, 128, 576] bf16; kv_cache [num_pages, 64, 576] bf16;
+    q [B, s_q, 128, 576] bf16; kv_cache [num_pages, 64, 576] bf16, or
+    uint8 [num_pages, 64, 656] FP8 rows (MLA_FLAG_KV_FP8 is then set);
     block_table [B, W] int32; cache_lens [B] int32; topk_idx [B, s_q, k]
     int32 or None.  bf16_pv selects MLA_FLAG_BF16_PV (two-token dense path:
     faster, less precise value product).  With validate=True the inputs are
@@ -100,6 +102,8 @@ def decode_step(q, kv_cache, block_table, cache_lens, softmax_scale: float, *, c
     topk = 0 if topk_idx is None else topk_idx.shape[-1]
     flags = (MLA_FLAG_CAUSAL if causal else 0) | (MLA_FLAG_OUT_FP32 if out_fp32 else 0) | (
         MLA_FLAG_VALIDATE if validate else 0) | (MLA_FLAG_BF16_PV if bf16_pv else 0)
+    if kv_cache.dtype == torch.uint8:
+        flags |= MLA_FLAG_KV_FP8
     mla_decode_plan(cache_lens, B, s_q, topk, U, workspace.buf, workspace.nbytes, stream)
     mla_decode(q, kv_cache, kv_cache.shape[0], block_table, block_table.stride(0), cache_lens, B, s_q,
                NUM_HEADS, softmax_scale, topk_idx, topk, flags, U, workspace.buf, workspace.nbytes, out,

@@ -29,6 +29,7 @@ MLA_FLAG_CAUSAL = 1
 MLA_FLAG_OUT_FP32 = 2
 MLA_FLAG_VALIDATE = 4
 MLA_FLAG_BF16_PV = 8
+MLA_FLAG_KV_FP8 = 16
 
 # every symbol the headers in include/ declare: name -> (restype, argtypes)
 _c_int, _c_size, _vp, _i64, _f32, _uint = (ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p,

@@ -24,11 +24,11 @@ __global__ void mla_validate_kernel(const int* lens, const int* bt, long long bt
                                     long long num_pages, int B, int s_q, const int* topk_idx, int topk,
                                     const uint16_t* kv, int check_range, int* status);
 int decode_smem_bytes();
-int decode_threads(bool sparse);
+int decode_threads(bool sparse, bool fp8);
 cudaError_t decode_set_attrs();
 cudaError_t decode_max_clusters(int* n, int num_clusters_hint);
-cudaError_t decode_launch(bool sparse, int num_clusters, cudaStream_t stream, const DecodeParams& p,
-                          const CUtensorMap& tm_q, const CUtensorMap& tm_kv);
+cudaError_t decode_launch(bool sparse, bool fp8, int num_clusters, cudaStream_t stream, const DecodeParams& p,
+                          const CUtensorMap& tm_q, const CUtensorMap& tm_kv, const CUtensorMap& tm_rope);
 cudaError_t mtp_set_attrs();
 cudaError_t mtp_max_clusters(int* n, int num_clusters_hint);
 cudaError_t mtp_launch(bool bf16_pv, int num_clusters, cudaStream_t stream, const DecodeParams& p,
@@ -160,6 +160,30 @@ int encode_kv_3d(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_c
   return r == CUDA_SUCCESS ? MLA_OK : MLA_ERR_CUDA;
 }
 
+// An FP8 cache (656-byte rows) for the one-token kernel: `lat` maps each row's
+// first 528 bytes (512 E4M3 codes, the scale bytes) as 132 32-bit words, one
+// 64-row box per tile, landing unswizzled; `rope` maps the row as 328 bf16
+// elements, a box of 64 of them (the RoPE dims, from element 264 = byte 528)
+// by 64 rows, 128B-swizzled like every chunk of the bf16 path.
+int encode_fp8_kv(CUtensorMap* lat, CUtensorMap* rope, const void* base, uint64_t rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return MLA_ERR_CUDA;
+  const cuuint64_t strides[1] = {656};
+  const cuuint32_t estr[2] = {1, 1};
+  const cuuint64_t dl[2] = {164, static_cast<cuuint64_t>(rows)};
+  const cuuint32_t bl[2] = {132, static_cast<cuuint32_t>(kPage)};
+  CUresult r = fn(lat, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(base), dl, strides, bl, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return MLA_ERR_CUDA;
+  const cuuint64_t dr[2] = {328, static_cast<cuuint64_t>(rows)};
+  const cuuint32_t br[2] = {static_cast<cuuint32_t>(kChunk), static_cast<cuuint32_t>(kPage)};
+  r = fn(rope, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dr, strides, br, estr,
+         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MLA_OK : MLA_ERR_CUDA;
+}
+
 // An output tensor of 512 columns per row (bf16 or fp32) for tensor stores of
 // 32-row boxes of 64-byte rows (32 bf16 or 16 fp32 columns), staged with the
 // 64-byte swizzle as the two-token kernel writes them.
@@ -263,9 +287,12 @@ int mla::check_decode_args(const void* q, const void* kv_cache, int64_t num_page
   if (!q || !kv_cache || !block_table || !cache_lens || !out || !lse) return MLA_ERR_INVALID_ARG;
   if (batch < 1 || num_pages < 1 || bt_stride < 1 || topk < 0) return MLA_ERR_INVALID_ARG;
   if ((topk_idx == nullptr) != (topk == 0)) return MLA_ERR_INVALID_ARG;
-  if (flags & ~static_cast<unsigned>(MLA_FLAG_CAUSAL | MLA_FLAG_OUT_FP32 | MLA_FLAG_VALIDATE | MLA_FLAG_BF16_PV))
+  if (flags & ~static_cast<unsigned>(MLA_FLAG_CAUSAL | MLA_FLAG_OUT_FP32 | MLA_FLAG_VALIDATE | MLA_FLAG_BF16_PV |
+                                     MLA_FLAG_KV_FP8))
     return MLA_ERR_INVALID_ARG;
   if (num_heads != kHeads || s_q < 1 || s_q > MLA_MAX_SQ) return MLA_ERR_UNSUPPORTED;
+  // an FP8 cache runs on the one-token kernel: not the two-token dense path
+  if ((flags & MLA_FLAG_KV_FP8) && plan_tile_rows(s_q, topk) == 128) return MLA_ERR_UNSUPPORTED;
   if (!std::isfinite(softmax_scale) || !(softmax_scale > 0.f)) return MLA_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(out, 16) || !aligned(lse, 4) ||
       !aligned(block_table, 4) || !aligned(cache_lens, 4) || (topk_idx && !aligned(topk_idx, 4)))
@@ -300,7 +327,8 @@ int mla_decode(const void* q, const void* kv_cache, int64_t num_pages, const int
     // attention and combine kernels then leave their outputs unwritten, and
     // mla_workspace_status reports the code (no host synchronisation here)
     int* status = reinterpret_cast<int*>(ws + L.hdr) + kHdrStatus;
-    const int check_range = (pair_path && (flags & MLA_FLAG_BF16_PV)) ? 0 : 1;  // fp16 value product
+    // the fp16 value product: bf16 values (1) or FP8 rows (2) below 65536
+    const int check_range = (flags & MLA_FLAG_KV_FP8) ? 2 : (pair_path && (flags & MLA_FLAG_BF16_PV)) ? 0 : 1;
     mla_validate_kernel<<<batch < 1024 ? batch : 1024, 256, 0, s>>>(
         cache_lens, block_table, bt_stride, num_pages, batch, s_q, topk_idx, topk,
         static_cast<const uint16_t*>(kv_cache), check_range, status);
@@ -333,11 +361,18 @@ int mla_decode(const void* q, const void* kv_cache, int64_t num_pages, const int
   p.part_bf16 = (flags & MLA_FLAG_BF16_PV) ? 1 : 0;
 
   // the two-token kernel moves Q through its 8 KiB chunk slots: 64-row boxes
-  CUtensorMap tm_q, tm_kv;
+  const bool fp8 = (flags & MLA_FLAG_KV_FP8) != 0;
+  CUtensorMap tm_q, tm_kv, tm_rope;
   if ((rc = encode_2d(&tm_q, q, static_cast<uint64_t>(batch) * s_q * kHeads, pair_path ? kPage : kHeads)) !=
       MLA_OK)
     return rc;
-  if ((rc = encode_2d(&tm_kv, kv_cache, static_cast<uint64_t>(num_pages) * kPage, kPage)) != MLA_OK) return rc;
+  if (fp8) {
+    if ((rc = encode_fp8_kv(&tm_kv, &tm_rope, kv_cache, static_cast<uint64_t>(num_pages) * kPage)) != MLA_OK)
+      return rc;
+  } else {
+    if ((rc = encode_2d(&tm_kv, kv_cache, static_cast<uint64_t>(num_pages) * kPage, kPage)) != MLA_OK) return rc;
+    tm_rope = tm_kv;  // unused by the bf16 kernels
+  }
 
   // two query tokens, dense: both tokens share every tile (4-CTA clusters,
   // paired-SM MMAs); otherwise one 2-CTA cluster per (unit, token)
@@ -354,7 +389,7 @@ int mla_decode(const void* q, const void* kv_cache, int64_t num_pages, const int
       return rc;
     e = mtp_launch((flags & MLA_FLAG_BF16_PV) != 0, U, s, p, tm_q, tm_k3, tm_v2, tm_out, tm_part);
   } else {
-    e = decode_launch(topk_idx != nullptr, U * s_q, s, p, tm_q, tm_kv);
+    e = decode_launch(topk_idx != nullptr, fp8, U * s_q, s, p, tm_q, tm_kv, tm_rope);
   }
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -366,7 +401,8 @@ int mla_decode(const void* q, const void* kv_cache, int64_t num_pages, const int
 int mla_combine(void* workspace, size_t ws_bytes, int batch, int s_q, int num_heads, unsigned flags,
                 int num_units, void* out, float* lse, mla_stream_t stream) {
   if (!workspace || !out || !lse || batch < 1) return MLA_ERR_INVALID_ARG;
-  if (flags & ~static_cast<unsigned>(MLA_FLAG_CAUSAL | MLA_FLAG_OUT_FP32 | MLA_FLAG_VALIDATE | MLA_FLAG_BF16_PV))
+  if (flags & ~static_cast<unsigned>(MLA_FLAG_CAUSAL | MLA_FLAG_OUT_FP32 | MLA_FLAG_VALIDATE | MLA_FLAG_BF16_PV |
+                                     MLA_FLAG_KV_FP8))
     return MLA_ERR_INVALID_ARG;
   if (num_heads != kHeads || s_q < 1 || s_q > MLA_MAX_SQ) return MLA_ERR_UNSUPPORTED;
   if (!aligned(out, 16) || !aligned(lse, 4) || !aligned(workspace, 256)) return MLA_ERR_INVALID_ARG;

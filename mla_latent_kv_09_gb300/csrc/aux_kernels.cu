@@ -225,8 +225,11 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(const int* __restrict_
 // ------------------------------------------------------------------ validate
 // Checks lengths, the block-table entries the step will read and the top-k
 // indices, and (check_range) that every value dim the step reads is finite
-// and converts to fp16 without overflow, i.e. |v| < 65536 as a bf16 pattern
-// below 0x4780; records the first problem found in the status word.  One
+// and converts to fp16 without overflow: check_range 1, a bf16 cache, |v| <
+// 65536 as a bf16 pattern below 0x4780; check_range 2, an FP8 cache (656-byte
+// rows), no NaN code, no scale byte 255, and |code| * scale < 65536 (every
+// such value is at most 61440); records the first problem found in the
+// status word.  One
 // CTA per request (grid-strided); reading the value dims of every visible row
 // makes this a full pass over the visible cache.
 __global__ void mla_validate_kernel(const int* __restrict__ lens, const int* __restrict__ bt,
@@ -237,6 +240,25 @@ __global__ void mla_validate_kernel(const int* __restrict__ lens, const int* __r
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
   // value dims 0..511 of pool row `row`: one warp, 16 B per lane, 2 rounds
   auto row_in_range = [&](long long row) {
+    if (check_range == 2) {  // FP8 row: lane l holds codes 16 l .. 16 l + 15 (scale group l / 8)
+      const uint8_t* r8 = reinterpret_cast<const uint8_t*>(kv) + row * 656;
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(r8) + lane);
+      const uint32_t eb = __ldg(r8 + 512 + (lane >> 3));
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      bool ok = eb != 255u;
+      float mx = 0.f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const uint32_t c = (w[i >> 2] >> (8 * (i & 3))) & 0x7fu;  // magnitude bits
+        const uint32_t e = c >> 3, m = c & 7u;
+        ok = ok && c != 0x7fu;
+        // E4M3 magnitude: (1 + m/8) 2^(e-7), or m 2^-9 for e = 0
+        const float a = e ? __uint_as_float(((e + 120u) << 23) | (m << 20)) : static_cast<float>(m) * 0.001953125f;
+        mx = fmaxf(mx, a);
+      }
+      const float s = eb ? __uint_as_float(eb << 23) : __uint_as_float(0x00400000u);
+      return __all_sync(0xffffffffu, ok && mx * s < 65536.f);
+    }
     const uint4* src = reinterpret_cast<const uint4*>(kv + row * kDqk);
     bool ok = true;
 #pragma unroll

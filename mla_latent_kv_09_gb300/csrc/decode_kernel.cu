@@ -37,6 +37,21 @@
 // 0-3 O correction + epilogue (thread i = head row i = TMEM lane i), 4-7 and
 // 10-11 V conversion (dense) or 4-7 and 10-15 row gather + conversion
 // (top-k), 8 MMA issue, 9 TMA producer (dense).
+//
+// FP8 latent cache (kFp8, MLA_FLAG_KV_FP8; 512 threads): a cached token is a
+// 656-byte row of 512 E4M3 latent dims, four UE8M0 (power-of-two) scales,
+// one per 128-dim group, and the 64 RoPE dims in bf16.  A tile's latent and
+// scale bytes (64 rows x 528 B) land at the end of the stage's eight latent
+// chunks (TMA, or the top-k row gather) and fill warps widen them in place:
+// every fill thread first reads its share of the raw bytes into registers,
+// the group meets at a named barrier, then each thread writes its pieces as
+// bf16 (S side, the score operand) or fp16 (O side, the value operand) in the
+// 128B-swizzled chunk layout.  A code times its power-of-two scale is exact
+// in bf16, and in fp16 below 65504, so the attention reads exactly the cached
+// values.  The S side's RoPE chunk lands directly in chunk 8.  Fill warps: S
+// side 10-15 (dense, warp 9 issues the TMA loads) or 9-15 (top-k), O side
+// 4-7 and 10-15; the MMA thread waits for the fill threads' arrivals (kVR)
+// on every ring slot, Q slots included.
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -52,6 +67,20 @@ constexpr int kStageS = kNumChunks * kChunkBytes;  // 9 chunks: all 576 dims
 constexpr int kStageO = 8 * kChunkBytes;           // 8 chunks: the 512 value dims
 constexpr int kPBytes = kHeads * 128;              // 128 rows x 64 fp16
 constexpr int kQChunkBytes = kHeads * 128;         // Q: 128 rows x 64 bf16, 128B-swizzled
+
+// FP8 latent cache: a row's latent + scale bytes (528 of 656) land at the
+// end of the eight latent chunks of a stage and are widened there.
+constexpr int kF8Row = 656;                                // bytes per cached token
+constexpr int kF8Lat = 528;                                // 512 E4M3 codes, 4 scale bytes, 12 unused
+constexpr int kF8RawBytes = kF8Lat * kPage;                // 33,792 per tile
+constexpr int kF8RawOff = 8 * kChunkBytes - kF8RawBytes;   // 31,744
+constexpr int kF8Pieces = 8 * kPage * 4;                   // 16-byte raw pieces (16 codes) per tile
+constexpr int kF8PerThread = (kF8Pieces + 191) / 192;      // 11: the fewest fill threads (S side, dense)
+static_assert(kF8RawOff % 16 == 0, "TMA destination alignment");
+// fill threads: S side warps 10-15 (dense) or 9-15 (top-k); O side 4-7, 10-15
+__host__ __device__ constexpr int f8_fill_threads(bool sparse, bool s_side) {
+  return s_side ? (sparse ? 224 : 192) : 320;
+}
 
 // Shared-memory layout (offsets from a 1024-aligned base).  The barrier block
 // sits at the same offset in both CTAs (multicast commits rely on it).
@@ -122,6 +151,34 @@ __device__ __forceinline__ void umma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem
       ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
 }
 
+// Two E4M3 codes (bits 0-7: the lower dim) -> fp16x2 (exact: every E4M3
+// value is an fp16 normal or zero).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
+  uint32_t r;
+  asm("{\n .reg .b16 c;\n cvt.u16.u32 c, %1;\n cvt.rn.f16x2.e4m3x2 %0, c;\n}" : "=r"(r) : "r"(two_codes));
+  return r;
+}
+
+// fp16x2 times a power-of-two scale -> bf16x2 (S side) or fp16x2 (O side).
+template <bool kToBf16>
+__device__ __forceinline__ uint32_t scale_f16x2(uint32_t h2, float s) {
+  float lo, hi;
+  asm("{\n .reg .f16 a, b;\n mov.b32 {a, b}, %2;\n cvt.f32.f16 %0, a;\n cvt.f32.f16 %1, b;\n}"
+      : "=f"(lo), "=f"(hi) : "r"(h2));
+  return kToBf16 ? pack_bf16x2(lo * s, hi * s) : pack_f16x2(lo * s, hi * s);
+}
+
+// UE8M0 byte -> 2^(byte - 127) as fp32 (byte 0 is the subnormal 2^-127).
+__device__ __forceinline__ float ue8m0_scale(uint32_t byte) {
+  return byte ? __uint_as_float(byte << 23) : __uint_as_float(0x00400000u);
+}
+
+__device__ __forceinline__ uint32_t ld_shared_u8(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.u8 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+  return v;
+}
+
 // Commit that arrives on the mbarrier at the same offset in every CTA of `mask`.
 __device__ __forceinline__ void umma_commit_multicast(uint32_t bar, uint16_t mask) {
   asm volatile(
@@ -135,10 +192,10 @@ __host__ __device__ constexpr uint32_t p_message_bytes(bool last) {
   return static_cast<uint32_t>(kPBytes + kHeads * 4 + (last ? kHeads * 4 : 0));
 }
 
-template <bool kSparse>
-__global__ void __launch_bounds__(kSparse ? kThreadsSparse : kThreads, 1)
+template <bool kSparse, bool kFp8>
+__global__ void __launch_bounds__((kSparse || kFp8) ? kThreadsSparse : kThreads, 1)
 mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tm_q,
-                  const __grid_constant__ CUtensorMap tm_kv) {
+                  const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_rope) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t mis = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* smem = smem_raw + mis;
@@ -182,7 +239,7 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
     for (int i = 0; i < kStages; ++i) {
       mbar_init(bar(kKF + i), 1);
       mbar_init(bar(kKE + i), 1);
-      mbar_init(bar(kVR + i), conv_threads(kSparse));
+      mbar_init(bar(kVR + i), kFp8 ? f8_fill_threads(kSparse, s_side) : conv_threads(kSparse));
     }
     mbar_init(bar(kQF), 1);
     for (int i = 0; i < 2; ++i) {
@@ -207,6 +264,7 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
   if (warp == 9 && lane == 0) {
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_kv);
+    if (kFp8 && s_side) tma_prefetch_desc(&tm_rope);
   }
   tc_fence_before();
   __syncthreads();
@@ -495,7 +553,7 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
           // once the previous segment's score MMAs have read the old Q
           if (nseg > 0 && !(ok = wait_bar<false>(bar(kQF), (nseg - 1u) & 1u, ctl))) break;
           for (int k = 0; k < 3 && ok; ++k, rs.advance()) {
-            if (!(ok = wait_bar<false>(bar(kKF + rs.idx), rs.phase, ctl))) break;
+            if (!(ok = wait_bar<false>(bar((kFp8 ? kVR : kKF) + rs.idx), rs.phase, ctl))) break;
             tc_fence_after();
             const uint64_t qd0 = smem_desc(sStage + rs.idx * stage_bytes, 16u, 1024u);
 #pragma unroll
@@ -513,7 +571,8 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
           const uint32_t stg = sStage + rs.idx * stage_bytes;
           const uint32_t sb = g & 1u, ph = (g >> 1) & 1u;
           if (s_side) {
-            if (!(ok = wait_bar<false>(bar(kKF + rs.idx), rs.phase, ctl))) break;
+            // the tile landed (bf16), or was widened by the fill threads (FP8)
+            if (!(ok = wait_bar<false>(bar((kFp8 ? kVR : kKF) + rs.idx), rs.phase, ctl))) break;
             if (kSparse) fence_proxy_async_smem();  // rows written by the gather threads' copies
             if (!(ok = wait_bar<false>(bar(kSE + sb), ph ^ 1u, ctl))) break;
             tc_fence_after();
@@ -604,10 +663,16 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
           if (lane == 0) {
             // an entry outside the pool reads the TMA fill value (zeros)
             const int y = page >= 0 ? page * kPage : static_cast<int>(p.num_pages) * kPage;
-            mbar_arrive_expect_tx(bar(kKF + rs.idx), nchunks * kChunkBytes);
-            for (int c = 0; c < nchunks; ++c)
-              tma_load_2d(sStage + rs.idx * stage_bytes + c * kChunkBytes, &tm_kv, c * kChunk, y,
-                          bar(kKF + rs.idx));
+            const uint32_t stg = sStage + rs.idx * stage_bytes;
+            if (kFp8) {  // latent + scale bytes to the stage's end; the S side's RoPE chunk to chunk 8
+              mbar_arrive_expect_tx(bar(kKF + rs.idx), kF8RawBytes + (s_side ? kChunkBytes : 0));
+              tma_load_2d(stg + kF8RawOff, &tm_kv, 0, y, bar(kKF + rs.idx));
+              if (s_side) tma_load_2d(stg + 8 * kChunkBytes, &tm_rope, kF8Lat / 2, y, bar(kKF + rs.idx));
+            } else {
+              mbar_arrive_expect_tx(bar(kKF + rs.idx), nchunks * kChunkBytes);
+              for (int c = 0; c < nchunks; ++c)
+                tma_load_2d(stg + c * kChunkBytes, &tm_kv, c * kChunk, y, bar(kKF + rs.idx));
+            }
           }
           ++issued;
         }
@@ -629,7 +694,169 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
     Seg sg;
     Ring3 rs;
     bool ok = true;
-    if ((!kSparse && s_side) || (kSparse && !s_side && warp == 9)) {
+    if (kFp8) {
+      if (!(kSparse && !s_side && warp == 9)) {
+        // ---- FP8 cache: fill threads widen each tile's codes in place
+        const int nthreads = f8_fill_threads(kSparse, s_side);
+        const int fid = s_side ? threadIdx.x - (kSparse ? 288 : 320) : ptid;  // 0 .. nthreads - 1
+        const uint8_t* kv8 = reinterpret_cast<const uint8_t*>(p.kv);
+        // Stage `stg`'s raw bytes (64 rows x 528 at kF8RawOff) -> bf16 (S
+        // side) / fp16 (O side) chunks 0-7.  Raw piece P (16 codes) is row
+        // (P >> 2) & 63, dims 64 (P >> 8) + 16 (P & 3) ..; its output is
+        // pieces 2 (P & 3) and 2 (P & 3) + 1 of that row in chunk P >> 8.
+        // Rows >= r_end are written as zeros.  All reads happen before the
+        // group barrier, all writes after it (the output overwrites the raw
+        // bytes); the barrier also votes `ok`, its result returned.
+        auto convert = [&](uint32_t stg, int r_end, bool ok_in) -> bool {
+          const uint32_t raw = stg + kF8RawOff;
+          uint4 v[kF8PerThread];
+          uint32_t e[kF8PerThread];
+#pragma unroll
+          for (int k = 0; k < kF8PerThread; ++k) {
+            const int P = fid + nthreads * k;
+            if (P < kF8Pieces) {
+              const uint32_t rb = raw + static_cast<uint32_t>(((P >> 2) & 63) * kF8Lat);
+              v[k] = ld_shared_v4u(rb + static_cast<uint32_t>(64 * (P >> 8) + 16 * (P & 3)));
+              e[k] = ld_shared_u8(rb + 512u + static_cast<uint32_t>(P >> 9));
+            }
+          }
+          if (!named_bar_all(5, nthreads, ok_in)) return false;
+#pragma unroll
+          for (int k = 0; k < kF8PerThread; ++k) {
+            const int P = fid + nthreads * k;
+            if (P < kF8Pieces) {
+              const int r = (P >> 2) & 63;
+              const uint32_t h = static_cast<uint32_t>(P & 3);
+              const uint32_t o = stg + static_cast<uint32_t>((P >> 8) * kChunkBytes + r * 128);
+              const uint32_t sw = static_cast<uint32_t>(r & 7);
+              if (r >= r_end) {
+                st_shared_zero16(o + (((2u * h) ^ sw) << 4));
+                st_shared_zero16(o + (((2u * h + 1u) ^ sw) << 4));
+              } else {
+                const float s = ue8m0_scale(e[k]);
+                const uint32_t in[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+                uint32_t w[8];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  const uint32_t a = e4m3x2_to_f16x2(in[i] & 0xffffu), b = e4m3x2_to_f16x2(in[i] >> 16);
+                  w[2 * i] = s_side ? scale_f16x2<true>(a, s) : scale_f16x2<false>(a, s);
+                  w[2 * i + 1] = s_side ? scale_f16x2<true>(b, s) : scale_f16x2<false>(b, s);
+                }
+                st_shared_v4(o + (((2u * h) ^ sw) << 4), w[0], w[1], w[2], w[3]);
+                st_shared_v4(o + (((2u * h + 1u) ^ sw) << 4), w[4], w[5], w[6], w[7]);
+              }
+            }
+          }
+          fence_proxy_async_smem();  // generic writes, read next by the tensor core
+          return true;
+        };
+        if (!kSparse) {
+          // dense: warp 9 loads (TMA); the fill threads pass Q slots on and
+          // widen each tile (the O side zeroes rows past the cache end)
+          while (ok && it.next(sg)) {
+            if (s_side) {
+              for (int k = 0; k < 3; ++k, rs.advance()) {
+                ok = ok && warp_wait(bar(kKF + rs.idx), rs.phase, ctl);
+                if (ok) mbar_arrive(bar(kVR + rs.idx));
+              }
+            }
+            const int L = max(p.cache_lens[sg.b], 0);
+            for (int j = sg.t0; j < sg.t1; ++j, rs.advance()) {
+              ok = ok && warp_wait(bar(kKF + rs.idx), rs.phase, ctl);
+              if (!(ok = convert(sStage + rs.idx * stage_bytes, s_side ? kPage : L - j * 64, ok))) break;
+              mbar_arrive(bar(kVR + rs.idx));
+            }
+          }
+        } else {
+          // top-k: the fill threads gather the named rows' latent + scale
+          // bytes (and on the S side the RoPE dims, straight into chunk 8)
+          // with 16-byte cp.async copies, one row per warp at a time, and
+          // widen tile j - 1 after issuing tile j's copies.  Rows the list
+          // does not name (or outside the pool) are zero-filled: value 0.
+          const int nw = nthreads / 32;
+          const int gw = fid >> 5;
+          const int rows_w = (kPage - gw + nw - 1) / nw;
+          const int npc = s_side ? kF8Lat / 16 + 8 : kF8Lat / 16;  // 16-byte pieces per row
+          int pend = -1;
+          // kKF completes only for the Q slots here (tiles land by cp.async):
+          // the parity of its next phase is tracked per slot, not by the ring
+          uint32_t qpar = 0u;
+          while (ok && it.next(sg)) {
+            if (s_side) {  // three Q slots (TMA from one fill thread), passed on once landed
+              for (int k = 0; k < 3; ++k, rs.advance()) {
+                ok = ok && warp_wait(bar(kKE + rs.idx), rs.phase ^ 1u, ctl);
+                if (ok && fid == 0) {
+                  const int qy = (sg.b * p.s_q + tok) * kHeads;
+                  mbar_arrive_expect_tx(bar(kKF + rs.idx), 3 * kQChunkBytes);
+                  for (int i = 0; i < 3; ++i)
+                    tma_load_2d(sStage + rs.idx * stage_bytes + i * kQChunkBytes, &tm_q, (3 * k + i) * kChunk, qy,
+                                bar(kKF + rs.idx));
+                }
+                ok = ok && warp_wait(bar(kKF + rs.idx), (qpar >> rs.idx) & 1u, ctl);
+                qpar ^= 1u << rs.idx;
+                if (ok) mbar_arrive(bar(kVR + rs.idx));
+              }
+            }
+            const int L = max(p.cache_lens[sg.b], 0);
+            const long long bt_row = static_cast<long long>(sg.b) * p.s_q + tok;
+            const int* idx = p.topk_idx + bt_row * p.topk;
+            const int* tbl = p.block_table + static_cast<long long>(sg.b) * p.bt_stride;
+            auto lookup = [&](int j) -> long long {
+              long long pr = -1;
+              if (lane < rows_w) {
+                const int pos = j * 64 + gw + nw * lane;
+                if (pos < p.topk) {
+                  const int ix = __ldg(idx + pos);
+                  if (ix >= 0 && ix < L && (ix >> 6) < p.bt_stride) {
+                    const int pg = __ldg(tbl + (ix >> 6));
+                    if (pg >= 0 && pg < p.num_pages) pr = static_cast<long long>(pg) * kPage + (ix & 63);
+                  }
+                }
+              }
+              return pr;
+            };
+            long long my_row = lookup(sg.t0);
+            for (int j = sg.t0; j < sg.t1; ++j, rs.advance()) {
+              ok = ok && warp_wait(bar(kKE + rs.idx), rs.phase ^ 1u, ctl);
+              if (!(ok = named_bar_all(5, nthreads, ok))) break;
+              const uint32_t stg = sStage + rs.idx * stage_bytes;
+              for (int i = 0; i < rows_w; ++i) {
+                const long long prow = __shfl_sync(0xffffffffu, my_row, i);
+                const int r = gw + nw * i;
+                const uint8_t* src = kv8 + (prow >= 0 ? prow : 0) * kF8Row;
+                const uint32_t src_bytes = prow >= 0 ? 16u : 0u;  // 0: the copy writes zeros
+                for (int c16 = lane; c16 < npc; c16 += 32) {
+                  if (c16 < kF8Lat / 16) {
+                    cp_async_16_zfill(stg + kF8RawOff + r * kF8Lat + 16 * c16, src + 16 * c16, src_bytes);
+                  } else {
+                    const int q = c16 - kF8Lat / 16;  // RoPE piece q -> chunk 8, swizzled
+                    cp_async_16_zfill(stg + 8 * kChunkBytes + r * 128 + ((q ^ (r & 7)) << 4), src + kF8Lat + 16 * q,
+                                      src_bytes);
+                  }
+                }
+              }
+              if (j + 1 < sg.t1) my_row = lookup(j + 1);
+              cp_async_commit();
+              if (pend >= 0) {  // the previous tile: every thread's copies landed -> widen
+                cp_async_wait<1>();
+                named_bar_sync(5, nthreads);
+                if (!(ok = convert(sStage + pend * stage_bytes, kPage, ok))) break;
+                mbar_arrive(bar(kVR + pend));
+              }
+              pend = static_cast<int>(rs.idx);
+            }
+            if (ok && pend >= 0) {  // the segment's last tile
+              cp_async_wait<0>();
+              named_bar_sync(5, nthreads);
+              if (!(ok = convert(sStage + pend * stage_bytes, kPage, ok))) break;
+              mbar_arrive(bar(kVR + pend));
+              pend = -1;
+            }
+          }
+          cp_async_wait<0>();  // no copy outlives the CTA
+        }
+      }
+    } else if ((!kSparse && s_side) || (kSparse && !s_side && warp == 9)) {
       // nothing to do: the S side consumes TMA tiles as they land
     } else if (!kSparse) {
       // ---- O side, dense: 192 threads convert the landed bf16 value tile to fp16 in place
@@ -792,22 +1019,24 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
 
 // ------------------------------------------------------------------ host side
 int decode_smem_bytes() { return kSmemBytes; }
-int decode_threads(bool sparse) { return sparse ? kThreadsSparse : kThreads; }
+int decode_threads(bool sparse, bool fp8) { return (sparse || fp8) ? kThreadsSparse : kThreads; }
 
 cudaError_t decode_set_attrs() {
-  cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       kSmemBytes);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(mla_decode_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  const cudaFuncAttribute a = cudaFuncAttributeMaxDynamicSharedMemorySize;
+  cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel<false, false>, a, kSmemBytes);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(mla_decode_kernel<true, false>, a, kSmemBytes);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(mla_decode_kernel<false, true>, a, kSmemBytes);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(mla_decode_kernel<true, true>, a, kSmemBytes);
+  return e;
 }
 
 // `dependent`: may be scheduled while the previous kernel on the stream (the
 // plan) finishes (programmatic dependent launch).
 static void cluster_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, int num_clusters,
-                           cudaStream_t stream, bool sparse, bool dependent) {
+                           cudaStream_t stream, int threads, bool dependent) {
   cfg = cudaLaunchConfig_t{};
   cfg.gridDim = dim3(2 * num_clusters, 1, 1);
-  cfg.blockDim = dim3(decode_threads(sparse), 1, 1);
+  cfg.blockDim = dim3(threads, 1, 1);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -824,17 +1053,22 @@ static void cluster_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, i
 cudaError_t decode_max_clusters(int* n, int num_clusters_hint) {
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[2];
-  cluster_config(cfg, attr, num_clusters_hint, nullptr, false, false);
-  return cudaOccupancyMaxActiveClusters(n, mla_decode_kernel<false>, &cfg);
+  cluster_config(cfg, attr, num_clusters_hint, nullptr, decode_threads(false, false), false);
+  return cudaOccupancyMaxActiveClusters(n, mla_decode_kernel<false, false>, &cfg);
 }
 
-cudaError_t decode_launch(bool sparse, int num_clusters, cudaStream_t stream, const DecodeParams& p,
-                          const CUtensorMap& tm_q, const CUtensorMap& tm_kv) {
+// fp8: the cache is FP8 (tm_kv then maps each row's 528 latent + scale bytes,
+// tm_rope its 64 bf16 RoPE dims).
+cudaError_t decode_launch(bool sparse, bool fp8, int num_clusters, cudaStream_t stream, const DecodeParams& p,
+                          const CUtensorMap& tm_q, const CUtensorMap& tm_kv, const CUtensorMap& tm_rope) {
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[2];
-  cluster_config(cfg, attr, num_clusters, stream, sparse, true);
-  return sparse ? cudaLaunchKernelEx(&cfg, mla_decode_kernel<true>, p, tm_q, tm_kv)
-                : cudaLaunchKernelEx(&cfg, mla_decode_kernel<false>, p, tm_q, tm_kv);
+  cluster_config(cfg, attr, num_clusters, stream, decode_threads(sparse, fp8), true);
+  if (fp8)
+    return sparse ? cudaLaunchKernelEx(&cfg, mla_decode_kernel<true, true>, p, tm_q, tm_kv, tm_rope)
+                  : cudaLaunchKernelEx(&cfg, mla_decode_kernel<false, true>, p, tm_q, tm_kv, tm_rope);
+  return sparse ? cudaLaunchKernelEx(&cfg, mla_decode_kernel<true, false>, p, tm_q, tm_kv, tm_rope)
+                : cudaLaunchKernelEx(&cfg, mla_decode_kernel<false, false>, p, tm_q, tm_kv, tm_rope);
 }
 
 }  // namespace mla

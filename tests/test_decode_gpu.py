@@ -32,11 +32,15 @@ def _build():
 
 def run(w, out_fp32=True, num_units=0, validate=False, q=None, kv=None, table=None, topk_idx="same",
         bf16_pv=False):
+    ws = m.Workspace(w.batch, w.s_q, num_units, w.q.device)
+    ws.buf.fill_(0x7F)  # nothing the step leaves unwritten may pass as a result
     o, lse = m.decode_step(w.q if q is None else q, w.kv if kv is None else kv,
                            w.block_table if table is None else table, w.cache_lens, w.softmax_scale,
                            causal=w.causal, topk_idx=w.topk_idx if topk_idx == "same" else topk_idx,
-                           out_fp32=out_fp32, num_units=num_units, validate=validate, bf16_pv=bf16_pv)
+                           out_fp32=out_fp32, num_units=num_units, validate=validate, bf16_pv=bf16_pv,
+                           workspace=ws)
     torch.cuda.synchronize()
+    assert m.mla_workspace_status(ws.buf) == m.MLA_OK  # no device wait ran out
     return o.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64)
 
 

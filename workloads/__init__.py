@@ -40,7 +40,7 @@ _CHUNK_ELEMS = 1 << 26  # elements drawn per randn call
 class Workload:
     name: str
     q: torch.Tensor  # bf16 [B, s_q, H, 576]
-    kv: torch.Tensor  # bf16 [num_pages, 64, 576]
+    kv: torch.Tensor  # bf16 [num_pages, 64, 576], or uint8 [num_pages, 64, 656] FP8 rows
     block_table: torch.Tensor  # int32 [B, max_pages]
     cache_lens: torch.Tensor  # int32 [B]
     topk_idx: torch.Tensor | None  # int32 [B, s_q, k] or None
@@ -63,6 +63,10 @@ class Workload:
     def topk(self) -> int:
         return 0 if self.topk_idx is None else self.topk_idx.shape[-1]
 
+    @property
+    def kv_fp8(self) -> bool:
+        return self.kv.dtype == torch.uint8
+
 
 def _np_rng(seed: int, stream: int) -> np.random.Generator:
     return np.random.Generator(np.random.Philox(np.random.SeedSequence([seed, stream])))
@@ -82,10 +86,42 @@ def _randn_bf16(shape, seed: int, stream: int, device, scale: float = 1.0) -> to
     return out
 
 
+FP8_ROW = 656  # bytes of an FP8 cache row: 512 E4M3 codes, 4 UE8M0 scales, 12 unused, 64 bf16 RoPE dims
+
+
+def _fp8_pool(num_pages: int, seed: int, device, spike_rows=None) -> torch.Tensor:
+    """An FP8 cache pool uint8 [num_pages, 64, 656] whose values are N(0,1)
+    like the bf16 pool's, quantised the way a cache writer would: each
+    128-dim group gets a UE8M0 scale byte 121 + d, d drawn from {0, 1, 2}
+    (scales 2^-6 .. 2^-4), and its codes are N(0,1) draws times 2^(6 - d)
+    cast to E4M3 by torch (clamped to +-448).  RoPE dims N(0,1) in bf16, the
+    12 unused bytes zero.  spike_rows: pool rows whose four scale bytes get
+    +3 (values x 8, exact)."""
+    rows = num_pages * PAGE
+    pool = torch.zeros((rows, FP8_ROW), dtype=torch.uint8, device=device)
+    d = _np_rng(seed, 8).integers(0, 3, size=(rows, 4)).astype(np.uint8)
+    mult = torch.from_numpy(np.exp2(6.0 - d).astype(np.float32)).to(device)
+    g = torch.Generator(device=device)
+    g.manual_seed(seed * 1000003 + 7)
+    step = max(1, _CHUNK_ELEMS // 512)
+    for lo in range(0, rows, step):
+        hi = min(rows, lo + step)
+        x = torch.randn((hi - lo, 4, 128), generator=g, device=device, dtype=torch.float32)
+        x = (x * mult[lo:hi, :, None]).clamp_(-448.0, 448.0)
+        pool[lo:hi, :512] = x.reshape(hi - lo, 512).to(torch.float8_e4m3fn).view(torch.uint8)
+    sc = 121 + d
+    if spike_rows is not None and len(spike_rows):
+        sc[spike_rows] += 3
+    pool[:, 512:516] = torch.from_numpy(sc).to(device)
+    rope = _randn_bf16((rows, 64), seed, 9, device)
+    pool[:, 528:] = rope.view(torch.uint8)
+    return pool.view(num_pages, PAGE, FP8_ROW)
+
+
 def make_workload(name: str, lens, s_q: int = 1, causal: bool = False, *,
                   topk: int = 0, pad_range=(0, 0), spike_frac: float = 0.0,
                   shuffle: bool = True, extra_pages: int = 0, seed: int = 0,
-                  device="cpu", max_pages: int | None = None) -> Workload:
+                  device="cpu", max_pages: int | None = None, kv_fp8: bool = False) -> Workload:
     """Build one decode call's inputs.
 
     lens:        per-request cache lengths (tokens).
@@ -97,6 +133,7 @@ def make_workload(name: str, lens, s_q: int = 1, causal: bool = False, *,
                  random order; otherwise request b's pages are contiguous.
     extra_pages: unused pool pages appended (filled with data too).
     max_pages:   width of the block table; unused entries hold -1.
+    kv_fp8:      the pool is FP8 rows (see _fp8_pool) instead of bf16.
     """
     lens = np.asarray(lens, dtype=np.int64)
     B = lens.size
@@ -113,8 +150,14 @@ def make_workload(name: str, lens, s_q: int = 1, causal: bool = False, *,
         cursor += n
 
     q = _randn_bf16((B, s_q, H, D_QK), seed, 2, device)
-    kv = _randn_bf16((max(total, 1), PAGE, D_QK), seed, 3, device)
-    if spike_frac > 0:
+    if kv_fp8:
+        spikes = None
+        if spike_frac > 0:
+            spikes = np.nonzero(_np_rng(seed, 4).random(max(total, 1) * PAGE) < spike_frac)[0]
+        kv = _fp8_pool(max(total, 1), seed, device, spikes)
+    else:
+        kv = _randn_bf16((max(total, 1), PAGE, D_QK), seed, 3, device)
+    if spike_frac > 0 and not kv_fp8:
         rows = np.nonzero(_np_rng(seed, 4).random(kv.shape[0] * PAGE) < spike_frac)[0]
         idx = torch.from_numpy(rows).to(device)
         flat = kv.view(-1, D_QK)
@@ -145,7 +188,7 @@ CONFIGS = ("single", "uniform_b32", "mtp_b64", "long_b128", "sparse_b80")
 
 
 def make_config(name: str, seed: int = 0, device="cpu", batch: int | None = None,
-                length: int | None = None) -> Workload:
+                length: int | None = None, kv_fp8: bool = False) -> Workload:
     """One of the five named workloads; `batch` / `length` shrink it for tests.
 
     single       B=1, L=256 (4 pages, identity block table), s_q=1
@@ -157,34 +200,33 @@ def make_config(name: str, seed: int = 0, device="cpu", batch: int | None = None
                  the last 0..300 entries padded with -1
     mtp4_b64     (beyond the five) mtp_b64's requests with four causal query
                  tokens each: speculative decoding with three draft tokens
+    <name>_fp8   (or kv_fp8=True) the same over an FP8 cache of the same shape
+                 (the FP8 latent cache; see _fp8_pool)
     """
+    if name.endswith("_fp8"):
+        w = make_config(name[:-4], seed, device, batch, length, kv_fp8=True)
+        w.name = name
+        return w
+    kw = dict(seed=seed, device=device, kv_fp8=kv_fp8)
     if name == "single":
-        return make_workload(name, [length or 256], shuffle=False, seed=seed, device=device)
+        return make_workload(name, [length or 256], shuffle=False, **kw)
     if name == "uniform_b32":
         B = batch or 32
-        return make_workload(name, [length or 4096] * B, seed=seed, device=device)
-    if name == "mtp_b64":
+        return make_workload(name, [length or 4096] * B, **kw)
+    if name in ("mtp_b64", "mtp4_b64"):
         B = batch or 64
         top = length or 8192
         lens = _np_rng(seed, 6).integers(1, top + 1, size=B)
-        return make_workload(name, lens, s_q=2, causal=True, seed=seed, device=device,
-                             max_pages=(top + PAGE - 1) // PAGE)
-    if name == "mtp4_b64":
-        B = batch or 64
-        top = length or 8192
-        lens = _np_rng(seed, 6).integers(1, top + 1, size=B)
-        return make_workload(name, lens, s_q=4, causal=True, seed=seed, device=device,
-                             max_pages=(top + PAGE - 1) // PAGE)
+        return make_workload(name, lens, s_q=2 if name == "mtp_b64" else 4, causal=True,
+                             max_pages=(top + PAGE - 1) // PAGE, **kw)
     if name == "long_b128":
         B = batch or 128
-        return make_workload(name, [length or 32768] * B, spike_frac=0.05, seed=seed,
-                             device=device)
+        return make_workload(name, [length or 32768] * B, spike_frac=0.05, **kw)
     if name == "sparse_b80":
         B = batch or 80
         L = length or 65536
         k = min(2048, L)
-        return make_workload(name, [L] * B, topk=k, pad_range=(0, min(300, k)),
-                             seed=seed, device=device)
+        return make_workload(name, [L] * B, topk=k, pad_range=(0, min(300, k)), **kw)
     raise KeyError(name)
 
 
@@ -194,9 +236,12 @@ def bf16_bits(t: torch.Tensor) -> np.ndarray:
 
 
 def host_arrays(w: Workload):
-    """The workload as numpy arrays (bf16 as uint16 bits) for the oracle."""
+    """The workload as numpy arrays (bf16 as uint16 bits) for the oracle; an
+    FP8 pool comes as its uint8 rows under kv_fp8 (kv_bits is then None)."""
+    fp8 = w.kv_fp8
     return dict(
-        q_bits=bf16_bits(w.q), kv_bits=bf16_bits(w.kv),
+        q_bits=bf16_bits(w.q), kv_bits=None if fp8 else bf16_bits(w.kv),
+        kv_fp8=w.kv.cpu().numpy() if fp8 else None,
         block_table=w.block_table.cpu().numpy(), cache_lens=w.cache_lens.cpu().numpy(),
         softmax_scale=w.softmax_scale, causal=w.causal,
         topk_idx=None if w.topk_idx is None else w.topk_idx.cpu().numpy())
