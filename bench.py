@@ -165,6 +165,10 @@ def oracle_sample(w, host, reqs):
     """Run the fp64 oracle on requests `reqs` (all their query tokens)."""
     import oracle
     sel = [(b, t) for b in reqs for t in range(w.s_q)]
+    if host["kv_fp8"] is not None:  # an FP8 cache
+        oracle.mla_decode_fp8(host["q_bits"], host["kv_fp8"], host["block_table"], host["cache_lens"],
+                              host["softmax_scale"], causal=host["causal"], topk_idx=host["topk_idx"], select=sel)
+        return
     oracle.mla_decode(host["q_bits"], host["kv_bits"], host["block_table"], host["cache_lens"],
                       host["softmax_scale"], causal=host["causal"], topk_idx=host["topk_idx"], select=sel)
 
@@ -246,6 +250,8 @@ def time_step(m, w, args, dev, world, sampler=None):
     stream = torch.cuda.current_stream(dev)
     topk = w.topk
     flags = (m.MLA_FLAG_CAUSAL if w.causal else 0) | (m.MLA_FLAG_BF16_PV if args.bf16_pv else 0)
+    if w.kv_fp8:
+        flags |= m.MLA_FLAG_KV_FP8
     U = ws.num_units
 
     # every call goes to the stream current at call time (the capture stream
@@ -341,7 +347,8 @@ def roofline_of(w, r, pk, pk_kind, step_ms):
     host_lens = w.cache_lens.cpu().numpy()
     host_topk = None if w.topk_idx is None else w.topk_idx.cpu().numpy()
     flops = acc.step_flops(host_lens, w.s_q, w.causal, host_topk)
-    nbytes = acc.step_bytes(host_lens, w.s_q, w.causal, host_topk)
+    nbytes = acc.step_bytes(host_lens, w.s_q, w.causal, host_topk,
+                            row_bytes=acc.FP8_ROW_BYTES if w.kv_fp8 else acc.ROW_BYTES)
     ridge = pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)
     bound = "tensor" if flops / nbytes > ridge else "hbm"
     dec_s = r["dec_ms"] * 1e-3
@@ -641,6 +648,7 @@ def run_ours(args, world, rank, local):
         step_ms = max_over_ranks(r["step_ms"], world)
         rf = roofline_of(w, r, pk, pk_kind, step_ms)
         entry = {"batch": w.batch, "s_q": w.s_q, "causal": w.causal, "topk": w.topk, "num_units": r["num_units"],
+                 "kv_cache": "fp8 (656-byte rows: E4M3 latent, UE8M0 group scales, bf16 RoPE)" if w.kv_fp8 else "bf16",
                  "us_per_call": step_ms * 1e3, "us_per_call_host_launches": r["launch_ms"] * 1e3,
                  "us_decode_kernel": r["dec_ms"] * 1e3, "us_plan": r["plan_ms"] * 1e3,
                  "us_combine": r["comb_ms"] * 1e3, "algorithmic_gflop": rf["flops"] / 1e9,
@@ -776,7 +784,8 @@ def main():
                     help="seconds of oracle work for the headline workload's CPU baseline")
     ap.add_argument("--cpu-budget-other", type=float, default=4.0,
                     help="seconds of oracle work for each other workload's CPU baseline")
-    ap.add_argument("--also", default="single,uniform_b32,long_b128,sparse_b80,mtp4_b64",
+    ap.add_argument("--also", default="single,uniform_b32,long_b128,sparse_b80,mtp4_b64,"
+                                      "uniform_b32_fp8,long_b128_fp8,sparse_b80_fp8",
                     help="other workloads timed before the headline one (comma-separated; 'none' for none)")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -5,8 +5,9 @@ FLOPs follow the absorbed-MLA count of "DeepSeek V3/R1 Inference Efficiency
 and P@V = 2*bs*s'*n_head*c, i.e. 2*128*576 + 2*128*512 = 278,528 flops per
 (query token, visible cache token).
 
-Bytes are the minimum traffic: every visible latent row (576 bf16 = 1152 B)
-read once per request (both MTP tokens share it), plus per (request, query
+Bytes are the minimum traffic: every visible latent row (576 bf16 = 1152 B,
+or a 656-byte FP8 row) read once per request (both MTP tokens share it),
+plus per (request, query
 token) the 128x576 bf16 query block, the 128x512 output block and the 128
 fp32 LSE values, plus 4 B per block-table entry, top-k index and length
 read.  Partial results of split requests, L2 re-reads and duplicated work
@@ -20,6 +21,7 @@ import numpy as np
 H, D_QK, D_V, PAGE = 128, 576, 512, 64
 FLOPS_PER_QT = 2 * H * D_QK + 2 * H * D_V  # 278,528
 ROW_BYTES = D_QK * 2
+FP8_ROW_BYTES = 656  # 512 E4M3 codes, 4 scale bytes, 12 unused, 64 bf16 RoPE dims
 
 
 def visible_counts(cache_lens, s_q: int, causal: bool, topk_idx=None) -> np.ndarray:
@@ -37,7 +39,8 @@ def step_flops(cache_lens, s_q: int, causal: bool, topk_idx=None) -> int:
     return int(visible_counts(cache_lens, s_q, causal, topk_idx).sum()) * FLOPS_PER_QT
 
 
-def step_bytes(cache_lens, s_q: int, causal: bool, topk_idx=None, out_bytes_per_elem: int = 2) -> int:
+def step_bytes(cache_lens, s_q: int, causal: bool, topk_idx=None, out_bytes_per_elem: int = 2,
+               row_bytes: int = ROW_BYTES) -> int:
     lens = np.maximum(np.asarray(cache_lens, dtype=np.int64), 0)
     B = lens.size
     if topk_idx is not None:
@@ -53,7 +56,7 @@ def step_bytes(cache_lens, s_q: int, causal: bool, topk_idx=None, out_bytes_per_
         table = int(((lens + PAGE - 1) // PAGE).sum())
         extra = 0
     per_qt = H * D_QK * 2 + H * D_V * out_bytes_per_elem + H * 4
-    return int(rows * ROW_BYTES + B * s_q * per_qt + 4 * table + extra + 4 * B)
+    return int(rows * row_bytes + B * s_q * per_qt + 4 * table + extra + 4 * B)
 
 
 # Weight-absorption BMMs on either side of the attention ("DeepSeek V3/R1

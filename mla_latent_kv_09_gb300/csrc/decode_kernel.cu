@@ -38,20 +38,24 @@
 // 10-11 V conversion (dense) or 4-7 and 10-15 row gather + conversion
 // (top-k), 8 MMA issue, 9 TMA producer (dense).
 //
-// FP8 latent cache (kFp8, MLA_FLAG_KV_FP8; 512 threads): a cached token is a
+// FP8 latent cache (kFp8, MLA_FLAG_KV_FP8; 640 threads): a cached token is a
 // 656-byte row of 512 E4M3 latent dims, four UE8M0 (power-of-two) scales,
 // one per 128-dim group, and the 64 RoPE dims in bf16.  A tile's latent and
 // scale bytes (64 rows x 528 B) land at the end of the stage's eight latent
 // chunks (TMA, or the top-k row gather) and fill warps widen them in place:
 // every fill thread first reads its share of the raw bytes into registers,
 // the group meets at a named barrier, then each thread writes its pieces as
-// bf16 (S side, the score operand) or fp16 (O side, the value operand) in the
-// 128B-swizzled chunk layout.  A code times its power-of-two scale is exact
-// in bf16, and in fp16 below 65504, so the attention reads exactly the cached
-// values.  The S side's RoPE chunk lands directly in chunk 8.  Fill warps: S
-// side 10-15 (dense, warp 9 issues the TMA loads) or 9-15 (top-k), O side
-// 4-7 and 10-15; the MMA thread waits for the fill threads' arrivals (kVR)
-// on every ring slot, Q slots included.
+// fp16 in the 128B-swizzled chunk layout: one convert and one multiply by
+// the power-of-two scale per two codes.  Both products then run in fp16 over
+// the latent dims: the S side also widens Q's 512 latent dims to fp16 (once
+// per segment, in its ring slots); the RoPE dims stay bf16 in both operands
+// (the score MMAs of chunk 8 take the bf16 descriptor).  A code times its
+// scale is exact in fp16 within its range (values and query latent dims below
+// 65504 in magnitude), so the attention reads exactly the cached values.  Fill
+// warps: S side 10-19 (dense, warp 9 issues the TMA loads) or 9-19 (top-k),
+// O side 4-7 and 10-19; the MMA thread waits for the fill threads' arrivals
+// (kVR) on every ring slot, Q slots included.  (The fill work is latency-
+// bound: 20 warps, so that 10-14 of them fill, measured faster than 16.)
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -75,11 +79,14 @@ constexpr int kF8Lat = 528;                                // 512 E4M3 codes, 4 
 constexpr int kF8RawBytes = kF8Lat * kPage;                // 33,792 per tile
 constexpr int kF8RawOff = 8 * kChunkBytes - kF8RawBytes;   // 31,744
 constexpr int kF8Pieces = 8 * kPage * 4;                   // 16-byte raw pieces (16 codes) per tile
-constexpr int kF8PerThread = (kF8Pieces + 191) / 192;      // 11: the fewest fill threads (S side, dense)
+constexpr int kF8Low = 3 * kPage * 4;                      // pieces of chunks 0-2: outputs below the raw bytes
+constexpr int kF8PerThread = (kF8Pieces - kF8Low + 319) / 320;  // 4: buffered pieces of chunks 3-7 per thread
 static_assert(kF8RawOff % 16 == 0, "TMA destination alignment");
-// fill threads: S side warps 10-15 (dense) or 9-15 (top-k); O side 4-7, 10-15
+// FP8 kernels run 20 warps; fill threads: S side warps 10-19 (dense) or 9-19
+// (top-k); O side 4-7 and 10-19
+constexpr int kThreadsFp8 = 640;
 __host__ __device__ constexpr int f8_fill_threads(bool sparse, bool s_side) {
-  return s_side ? (sparse ? 224 : 192) : 320;
+  return s_side ? (sparse ? 352 : 320) : 448;
 }
 
 // Shared-memory layout (offsets from a 1024-aligned base).  The barrier block
@@ -131,6 +138,9 @@ static_assert(kNumBars * 8 + 16 <= kBarBytes, "barrier block");
 // kind::f16 instruction descriptors: S = Q K^T with bf16 operands; O += P V
 // with fp16 operands (A and B of one MMA always share a type).
 constexpr uint32_t kIdescQK = idesc_bf16(128, 64, 0);
+// FP8 cache: the scores take Q and K in fp16 (A and B formats 0) over the
+// 512 latent dims, in bf16 over the 64 RoPE dims (chunk 8)
+constexpr uint32_t kIdescQK16 = kIdescQK & ~((1u << 7) | (1u << 10));
 constexpr uint32_t kIdescPV = (1u << 4) | (0u << 7) | (0u << 10) | (1u << 16) | ((256u >> 3) << 17) |
                               ((128u >> 4) << 24);
 
@@ -168,6 +178,57 @@ __device__ __forceinline__ uint32_t scale_f16x2(uint32_t h2, float s) {
   return kToBf16 ? pack_bf16x2(lo * s, hi * s) : pack_f16x2(lo * s, hi * s);
 }
 
+// The scale 2^(E - 127) of a UE8M0 byte as two fp16x2 multipliers m1 * m2:
+// m1 = 2^clamp(E - 127, -24, 15) (an fp16 power of two, subnormal below
+// 2^-14), m2 the rest (1 for E in [103, 142]; else a power of two that
+// underflows to 0 or overflows to infinity as fp16 would).
+__device__ __forceinline__ uint2 f16_scale_pair(uint32_t E) {
+  const int k = static_cast<int>(E) - 127;
+  const int k1 = k < -24 ? -24 : (k > 15 ? 15 : k);
+  const int k2 = k - k1;
+  auto pow2 = [](int e) -> uint32_t {  // 2^e as fp16 bits
+    if (e > 15) return 0x7c00u;
+    if (e >= -14) return static_cast<uint32_t>(e + 15) << 10;
+    if (e >= -24) return 1u << (e + 24);
+    return 0u;
+  };
+  const uint32_t m1 = pow2(k1), m2 = pow2(k2);
+  return make_uint2(m1 | (m1 << 16), m2 | (m2 << 16));
+}
+
+// 16 E4M3 codes (a raw piece, dims in byte order) times the scale (m) -> 8
+// fp16x2 words: one convert and one multiply (two outside [103, 142]) per two
+// codes.  Exact wherever the result is an fp16 (normal, or subnormal on its
+// 2^-24 grid), which covers |v| in [2^-14, 65504].  (Placing the code bits
+// with integer operations instead measured slower, also with 20 warps.)
+__device__ __forceinline__ void widen_f16(uint4 v, uint2 m, uint32_t (&w)[8]) {
+  const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t a, b;
+    asm("{\n .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %2;\n cvt.rn.f16x2.e4m3x2 %0, lo;\n cvt.rn.f16x2.e4m3x2 %1, hi;\n}"
+        : "=r"(a), "=r"(b) : "r"(in[i]));
+    asm("mul.rn.f16x2 %0, %0, %1;" : "+r"(a) : "r"(m.x));
+    asm("mul.rn.f16x2 %0, %0, %1;" : "+r"(b) : "r"(m.x));
+    if (m.y != 0x3c003c00u) {
+      asm("mul.rn.f16x2 %0, %0, %1;" : "+r"(a) : "r"(m.y));
+      asm("mul.rn.f16x2 %0, %0, %1;" : "+r"(b) : "r"(m.y));
+    }
+    w[2 * i] = a;
+    w[2 * i + 1] = b;
+  }
+}
+
+// In place: the 16-byte pieces piece0, piece0 + step, ... (< n) of the bf16
+// region at `base` -> fp16 (exact within fp16's range).
+__device__ __forceinline__ void bf16_region_to_f16(uint32_t base, int piece0, int step, int n) {
+  for (int i = piece0; i < n; i += step) {
+    const uint32_t a = base + 16u * static_cast<uint32_t>(i);
+    const uint4 v = ld_shared_v4u(a);
+    st_shared_v4(a, bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z), bf16x2_to_f16x2(v.w));
+  }
+}
+
 // UE8M0 byte -> 2^(byte - 127) as fp32 (byte 0 is the subnormal 2^-127).
 __device__ __forceinline__ float ue8m0_scale(uint32_t byte) {
   return byte ? __uint_as_float(byte << 23) : __uint_as_float(0x00400000u);
@@ -193,7 +254,7 @@ __host__ __device__ constexpr uint32_t p_message_bytes(bool last) {
 }
 
 template <bool kSparse, bool kFp8>
-__global__ void __launch_bounds__((kSparse || kFp8) ? kThreadsSparse : kThreads, 1)
+__global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : (kSparse ? kThreadsSparse : kThreads), 1)
 mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tm_q,
                   const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_rope) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -585,7 +646,8 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk)
                 umma_f16_tmem_a(dS, tmem + kColQ + 32u * c + 8u * kk,
-                                bd0 + static_cast<uint64_t>((c * kChunkBytes + 32 * kk) >> 4), kIdescQK,
+                                bd0 + static_cast<uint64_t>((c * kChunkBytes + 32 * kk) >> 4),
+                                (kFp8 && c < 8) ? kIdescQK16 : kIdescQK,
                                 (c | kk) != 0 ? 1u : 0u);
             }
             umma_commit(bar(kSF + sb));
@@ -700,52 +762,60 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
         const int nthreads = f8_fill_threads(kSparse, s_side);
         const int fid = s_side ? threadIdx.x - (kSparse ? 288 : 320) : ptid;  // 0 .. nthreads - 1
         const uint8_t* kv8 = reinterpret_cast<const uint8_t*>(p.kv);
-        // Stage `stg`'s raw bytes (64 rows x 528 at kF8RawOff) -> bf16 (S
-        // side) / fp16 (O side) chunks 0-7.  Raw piece P (16 codes) is row
-        // (P >> 2) & 63, dims 64 (P >> 8) + 16 (P & 3) ..; its output is
-        // pieces 2 (P & 3) and 2 (P & 3) + 1 of that row in chunk P >> 8.
-        // Rows >= r_end are written as zeros.  All reads happen before the
-        // group barrier, all writes after it (the output overwrites the raw
-        // bytes); the barrier also votes `ok`, its result returned.
+        // Stage `stg`'s raw bytes (64 rows x 528 at kF8RawOff) -> fp16
+        // chunks 0-7 (the S side's RoPE chunk 8 stays bf16).  Raw piece
+        // P (16 codes) is row (P >> 2) & 63, dims 64 (P >> 8) + 16 (P & 3) ..;
+        // its output is pieces 2 (P & 3) and 2 (P & 3) + 1 of that row in
+        // chunk P >> 8.  Rows >= r_end are written as zeros.  Chunks 0-2 end
+        // below the raw bytes and are written as they are read; chunks 3-7
+        // overwrite them, so every thread reads its pieces of those first and
+        // writes them after the group barrier (which also votes `ok`, the
+        // result returned).
         auto convert = [&](uint32_t stg, int r_end, bool ok_in) -> bool {
           const uint32_t raw = stg + kF8RawOff;
+          // widen raw piece P (codes v, scale byte E) and store its two output pieces
+          auto put = [&](int P, uint4 v, uint32_t E) {
+            const int r = (P >> 2) & 63;
+            const uint32_t h = static_cast<uint32_t>(P & 3);
+            const uint32_t o = stg + static_cast<uint32_t>((P >> 8) * kChunkBytes + r * 128);
+            const uint32_t sw = static_cast<uint32_t>(r & 7);
+            if (r >= r_end) {
+              st_shared_zero16(o + (((2u * h) ^ sw) << 4));
+              st_shared_zero16(o + (((2u * h + 1u) ^ sw) << 4));
+            } else {
+              uint32_t w[8];
+              widen_f16(v, f16_scale_pair(E), w);
+              st_shared_v4(o + (((2u * h) ^ sw) << 4), w[0], w[1], w[2], w[3]);
+              st_shared_v4(o + (((2u * h + 1u) ^ sw) << 4), w[4], w[5], w[6], w[7]);
+            }
+          };
+          auto raw_piece = [&](int P, uint4& v, uint32_t& E) {
+            const uint32_t rb = raw + static_cast<uint32_t>(((P >> 2) & 63) * kF8Lat);
+            v = ld_shared_v4u(rb + static_cast<uint32_t>(64 * (P >> 8) + 16 * (P & 3)));
+            E = ld_shared_u8(rb + 512u + static_cast<uint32_t>(P >> 9));
+          };
+          // chunks 3-7 overwrite raw bytes: this thread's pieces of them are
+          // read first, and written only after the group barrier
           uint4 v[kF8PerThread];
           uint32_t e[kF8PerThread];
 #pragma unroll
           for (int k = 0; k < kF8PerThread; ++k) {
-            const int P = fid + nthreads * k;
-            if (P < kF8Pieces) {
-              const uint32_t rb = raw + static_cast<uint32_t>(((P >> 2) & 63) * kF8Lat);
-              v[k] = ld_shared_v4u(rb + static_cast<uint32_t>(64 * (P >> 8) + 16 * (P & 3)));
-              e[k] = ld_shared_u8(rb + 512u + static_cast<uint32_t>(P >> 9));
-            }
+            const int P = kF8Low + fid + nthreads * k;
+            if (P < kF8Pieces) raw_piece(P, v[k], e[k]);
+          }
+          // chunks 0-2 lie below the raw bytes: streamed before the barrier
+#pragma unroll 2
+          for (int P = fid; P < kF8Low; P += nthreads) {
+            uint4 c;
+            uint32_t E;
+            raw_piece(P, c, E);
+            put(P, c, E);
           }
           if (!named_bar_all(5, nthreads, ok_in)) return false;
 #pragma unroll
           for (int k = 0; k < kF8PerThread; ++k) {
-            const int P = fid + nthreads * k;
-            if (P < kF8Pieces) {
-              const int r = (P >> 2) & 63;
-              const uint32_t h = static_cast<uint32_t>(P & 3);
-              const uint32_t o = stg + static_cast<uint32_t>((P >> 8) * kChunkBytes + r * 128);
-              const uint32_t sw = static_cast<uint32_t>(r & 7);
-              if (r >= r_end) {
-                st_shared_zero16(o + (((2u * h) ^ sw) << 4));
-                st_shared_zero16(o + (((2u * h + 1u) ^ sw) << 4));
-              } else {
-                const float s = ue8m0_scale(e[k]);
-                const uint32_t in[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
-                uint32_t w[8];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                  const uint32_t a = e4m3x2_to_f16x2(in[i] & 0xffffu), b = e4m3x2_to_f16x2(in[i] >> 16);
-                  w[2 * i] = s_side ? scale_f16x2<true>(a, s) : scale_f16x2<false>(a, s);
-                  w[2 * i + 1] = s_side ? scale_f16x2<true>(b, s) : scale_f16x2<false>(b, s);
-                }
-                st_shared_v4(o + (((2u * h) ^ sw) << 4), w[0], w[1], w[2], w[3]);
-                st_shared_v4(o + (((2u * h + 1u) ^ sw) << 4), w[4], w[5], w[6], w[7]);
-              }
-            }
+            const int P = kF8Low + fid + nthreads * k;
+            if (P < kF8Pieces) put(P, v[k], e[k]);
           }
           fence_proxy_async_smem();  // generic writes, read next by the tensor core
           return true;
@@ -757,7 +827,11 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
             if (s_side) {
               for (int k = 0; k < 3; ++k, rs.advance()) {
                 ok = ok && warp_wait(bar(kKF + rs.idx), rs.phase, ctl);
-                if (ok) mbar_arrive(bar(kVR + rs.idx));
+                if (ok) {  // Q's latent dims (bf16) -> fp16; its RoPE chunk (8, in slot 2) stays bf16
+                  bf16_region_to_f16(sStage + rs.idx * stage_bytes, fid, nthreads, (k < 2 ? 3 : 2) * kQChunkBytes / 16);
+                  fence_proxy_async_smem();
+                  mbar_arrive(bar(kVR + rs.idx));
+                }
               }
             }
             const int L = max(p.cache_lens[sg.b], 0);
@@ -794,7 +868,11 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
                 }
                 ok = ok && warp_wait(bar(kKF + rs.idx), (qpar >> rs.idx) & 1u, ctl);
                 qpar ^= 1u << rs.idx;
-                if (ok) mbar_arrive(bar(kVR + rs.idx));
+                if (ok) {  // Q's latent dims (bf16) -> fp16; its RoPE chunk (8, in slot 2) stays bf16
+                  bf16_region_to_f16(sStage + rs.idx * stage_bytes, fid, nthreads, (k < 2 ? 3 : 2) * kQChunkBytes / 16);
+                  fence_proxy_async_smem();
+                  mbar_arrive(bar(kVR + rs.idx));
+                }
               }
             }
             const int L = max(p.cache_lens[sg.b], 0);
@@ -1019,7 +1097,7 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
 
 // ------------------------------------------------------------------ host side
 int decode_smem_bytes() { return kSmemBytes; }
-int decode_threads(bool sparse, bool fp8) { return (sparse || fp8) ? kThreadsSparse : kThreads; }
+int decode_threads(bool sparse, bool fp8) { return fp8 ? kThreadsFp8 : (sparse ? kThreadsSparse : kThreads); }
 
 cudaError_t decode_set_attrs() {
   const cudaFuncAttribute a = cudaFuncAttributeMaxDynamicSharedMemorySize;

@@ -1,9 +1,9 @@
 """Parity of the FP8-cache decode path (MLA_FLAG_KV_FP8) against the fp64
 oracle over the same FP8 rows, with the bar of the bf16 path: O max-abs
 <= 2e-2, mean-abs <= 2e-3, LSE <= 1e-3 (GPU required).  Because the rows'
-power-of-two scales make every cached value exact in bf16 (and in fp16 in
-range), the FP8 path must also give bit-for-bit the output of the bf16 path
-on a bf16 cache holding the same values."""
+power-of-two scales make every cached value exact in fp16 within its range,
+the FP8 path must also agree to 1e-5 with the bf16 path on a bf16 cache
+holding the same values."""
 
 import numpy as np
 import pytest
@@ -92,11 +92,16 @@ def test_small_workloads(name, kw):
 
 
 @pytest.mark.parametrize("name", ["single_fp8", "uniform_b32_fp8", "sparse_b80_fp8", "mtp4_b64_fp8"])
-def test_bit_identical_to_the_bf16_path_on_the_same_values(name):
+def test_matches_the_bf16_path_on_the_same_values(name):
+    # the same cached values through the bf16 path: both value products are
+    # fp16 on the same values; the FP8 path's scores take Q and K in fp16,
+    # where a bf16 query dim below 2^-14 in magnitude rounds to an fp16
+    # subnormal (an absolute change under 2^-25): agreement to 1e-5, where a
+    # misplaced dim or scale would cost O(1)
     w = wl.make_config(name, device="cuda", batch=3, length=900)
     o8, l8 = run(w)
     o16, l16 = run(w, kv=bf16_copy(w))
-    assert np.array_equal(o8, o16) and np.array_equal(l8, l16)
+    assert np.abs(o8 - o16).max() <= 1e-5 and np.abs(l8 - l16).max() <= 1e-5
 
 
 FULL = [("uniform_b32_fp8", 6), ("long_b128_fp8", 3), ("sparse_b80_fp8", 4)]
