@@ -114,11 +114,13 @@ enum {
  *                     scale = 2^(byte - 127)
  *   bytes [516, 528)  unused
  *   bytes [528, 656)  the 64 RoPE dims in bf16
- * Latent dim d = e4m3(byte d) * scale[d / 128].  Power-of-two scales make
- * every such value exact in bf16 (the score operand) and, below 65504 in
- * magnitude, in fp16 (the value operand), so the step attends over exactly
- * the values the rows encode.  A page is 64 rows (41,984 bytes); the block
- * table is unchanged.
+ * Latent dim d = e4m3(byte d) * scale[d / 128].  With an FP8 cache both
+ * products take the latent dims in fp16 (the query's too; the RoPE dims stay
+ * bf16): power-of-two scales make every cached value exact in fp16 within
+ * its range, so the step attends over exactly the values the rows encode,
+ * provided the cached values and the query's latent dims stay below 65504 in
+ * magnitude (query dims below 2^-14 round to fp16 subnormals).  A page is 64
+ * rows (41,984 bytes); the block table is unchanged.
  */
 enum { MLA_FP8_ROW_BYTES = 656 };
 
