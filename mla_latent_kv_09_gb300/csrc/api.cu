@@ -370,8 +370,11 @@ int mla_decode(const void* q, const void* kv_cache, int64_t num_pages, const int
     if ((rc = encode_fp8_kv(&tm_kv, &tm_rope, kv_cache, static_cast<uint64_t>(num_pages) * kPage)) != MLA_OK)
       return rc;
   } else {
-    if ((rc = encode_2d(&tm_kv, kv_cache, static_cast<uint64_t>(num_pages) * kPage, kPage)) != MLA_OK) return rc;
-    tm_rope = tm_kv;  // unused by the bf16 kernels
+    // one-token kernel: a page's nine chunks (S side) / eight value chunks (O
+    // side) as one 3-D box each; the two-token kernel encodes its own maps
+    const uint64_t rows = static_cast<uint64_t>(num_pages) * kPage;
+    if ((rc = encode_kv_3d(&tm_kv, kv_cache, rows, kNumChunks)) != MLA_OK) return rc;
+    if ((rc = encode_kv_3d(&tm_rope, kv_cache, rows, 8)) != MLA_OK) return rc;
   }
 
   // two query tokens, dense: both tokens share every tile (4-CTA clusters,

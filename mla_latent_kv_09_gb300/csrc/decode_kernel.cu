@@ -325,7 +325,7 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
   if (warp == 9 && lane == 0) {
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_kv);
-    if (kFp8 && s_side) tma_prefetch_desc(&tm_rope);
+    tma_prefetch_desc(&tm_rope);
   }
   tc_fence_before();
   __syncthreads();
@@ -730,10 +730,9 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
               mbar_arrive_expect_tx(bar(kKF + rs.idx), kF8RawBytes + (s_side ? kChunkBytes : 0));
               tma_load_2d(stg + kF8RawOff, &tm_kv, 0, y, bar(kKF + rs.idx));
               if (s_side) tma_load_2d(stg + 8 * kChunkBytes, &tm_rope, kF8Lat / 2, y, bar(kKF + rs.idx));
-            } else {
+            } else {  // the tile's nine (S side) or eight (O side) chunks as one 3-D box
               mbar_arrive_expect_tx(bar(kKF + rs.idx), nchunks * kChunkBytes);
-              for (int c = 0; c < nchunks; ++c)
-                tma_load_2d(stg + c * kChunkBytes, &tm_kv, c * kChunk, y, bar(kKF + rs.idx));
+              tma_load_3d(stg, s_side ? &tm_kv : &tm_rope, 0, y, 0, bar(kKF + rs.idx));
             }
           }
           ++issued;
@@ -1135,8 +1134,9 @@ cudaError_t decode_max_clusters(int* n, int num_clusters_hint) {
   return cudaOccupancyMaxActiveClusters(n, mla_decode_kernel<false, false>, &cfg);
 }
 
-// fp8: the cache is FP8 (tm_kv then maps each row's 528 latent + scale bytes,
-// tm_rope its 64 bf16 RoPE dims).
+// Maps: bf16 cache, tm_kv = a page's nine chunks (S side), tm_rope = its
+// eight value chunks (O side), as 3-D boxes; FP8 cache, tm_kv = each row's
+// 528 latent + scale bytes, tm_rope = its 64 bf16 RoPE dims.
 cudaError_t decode_launch(bool sparse, bool fp8, int num_clusters, cudaStream_t stream, const DecodeParams& p,
                           const CUtensorMap& tm_q, const CUtensorMap& tm_kv, const CUtensorMap& tm_rope) {
   cudaLaunchConfig_t cfg;
