@@ -346,6 +346,45 @@ def test_repeated_calls_are_bit_identical():
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
 
 
+# ---------------------------------------------------------------- split requests and their combine
+
+@pytest.mark.parametrize("s_q,causal,length,units", [(1, False, 64 * 300, 40), (2, True, 128 * 300, 36)])
+def test_a_request_split_over_more_than_32_units_is_combined(s_q, causal, length, units):
+    # more than 32 splits: the combine takes the weights of splits 32.. on its
+    # slow path (one lane holds one split's LSE); the short second request is whole
+    w = wl.make_workload("many", [length, 500], s_q=s_q, causal=causal, seed=31, device="cuda")
+    _, rm = m.mla_decode_plan_host(w.cache_lens.cpu().numpy(), s_q, 0, units)
+    assert rm[0, 1] > 32
+    o_ref, lse_ref = reference(w)
+    for out_fp32 in (True, False):
+        o, lse = run(w, num_units=units, out_fp32=out_fp32)
+        assert_close(o, lse, o_ref, lse_ref, bf16_scaled=not out_fp32)
+
+
+@pytest.mark.parametrize("s_q,causal,topk", [(1, False, 0), (2, True, 0), (2, False, 1024)])
+def test_decode_repeated_on_one_plan_gives_the_same_result(s_q, causal, topk):
+    # the plan is read-only to the attention and combine kernels: a second
+    # decode + combine on the same plan (no new mla_decode_plan) gives the
+    # same bits
+    w = wl.make_workload("rep", [5000, 2500, 700, 9000], s_q=s_q, causal=causal, topk=topk, seed=33,
+                         device="cuda")
+    o1, l1 = run(w)
+    ws = m.Workspace(w.batch, w.s_q, 0, w.q.device)
+    U = ws.num_units
+    flags = (m.MLA_FLAG_CAUSAL if causal else 0) | m.MLA_FLAG_OUT_FP32
+    B = w.batch
+    m.mla_decode_plan(w.cache_lens, B, s_q, topk, U, ws.buf, ws.nbytes)
+    for _ in range(2):
+        o = torch.full((B, s_q, 128, 512), float("nan"), device="cuda")
+        lse = torch.full((B, s_q, 128), float("nan"), device="cuda")
+        m.mla_decode(w.q, w.kv, w.kv.shape[0], w.block_table, w.block_table.stride(0), w.cache_lens, B, s_q,
+                     128, w.softmax_scale, w.topk_idx, topk, flags, U, ws.buf, ws.nbytes, o, lse)
+        m.mla_combine(ws.buf, ws.nbytes, B, s_q, 128, flags, U, o, lse)
+        torch.cuda.synchronize()
+        assert m.mla_workspace_status(ws.buf) == m.MLA_OK
+        assert np.array_equal(o.cpu().numpy(), o1) and np.array_equal(lse.cpu().numpy(), l1)
+
+
 def test_two_token_page_permutation_gives_identical_output():
     w = wl.make_config("mtp_b64", device="cuda", batch=3, length=900)
     o1, l1 = run(w)
