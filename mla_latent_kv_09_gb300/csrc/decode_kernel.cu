@@ -554,6 +554,10 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
           // combination of value rows, which the fp16 value product keeps
           // below 65504; bf16 with MLA_FLAG_BF16_PV), or final fp32 O
           const bool part = sg.slot >= 0;
+          // rows are 1 or 2 KiB apart: 32-byte stores wherever the base allows
+          // them (the workspace always does; the caller's output must be
+          // 16-byte aligned only)
+          const bool v8 = part || (reinterpret_cast<uintptr_t>(p.out) & 31u) == 0;
           if (part && sg.slot >= 2 * U) {
             // the plan never uses more than 2 * (U - 1) slots
           } else if (part || !p.out_fp32) {
@@ -577,8 +581,13 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
                 for (int c = 0; c < 16; ++c)
                   w[c] = pack_bf16x2(__uint_as_float(r[2 * c]) * fin, __uint_as_float(r[2 * c + 1]) * fin);
               }
+              if (v8) {  // whole 32-byte sectors
+                st_global_v8(dst, w);
+                st_global_v8(dst + 2, w + 8);
+              } else {
 #pragma unroll
-              for (int k = 0; k < 4; ++k) dst[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+                for (int k = 0; k < 4; ++k) dst[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+              }
             }
           } else {
             float* dst0 = static_cast<float*>(p.out) + (bt_row * kHeads + row) * kDv;
@@ -587,11 +596,18 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
               uint32_t r[32];
               tmem_ld32(tmem + lane_base + kColO + 32u * cc, r);
               tmem_wait_ld();
-              float4* dst = reinterpret_cast<float4*>(dst0 + 32 * cc);
 #pragma unroll
-              for (int k = 0; k < 8; ++k)
-                dst[k] = make_float4(__uint_as_float(r[4 * k]) * fin, __uint_as_float(r[4 * k + 1]) * fin,
-                                     __uint_as_float(r[4 * k + 2]) * fin, __uint_as_float(r[4 * k + 3]) * fin);
+              for (int c = 0; c < 32; ++c) r[c] = __float_as_uint(__uint_as_float(r[c]) * fin);
+              if (v8) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) st_global_v8(dst0 + 32 * cc + 8 * k, r + 8 * k);
+              } else {
+                float4* dst = reinterpret_cast<float4*>(dst0 + 32 * cc);
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                  dst[k] = make_float4(__uint_as_float(r[4 * k]), __uint_as_float(r[4 * k + 1]),
+                                       __uint_as_float(r[4 * k + 2]), __uint_as_float(r[4 * k + 3]));
+              }
             }
           }
           tc_fence_before();

@@ -346,6 +346,26 @@ def test_repeated_calls_are_bit_identical():
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
 
 
+@pytest.mark.parametrize("s_q,out_fp32", [(1, False), (1, True), (2, False)])
+def test_output_aligned_to_16_bytes_only(s_q, out_fp32):
+    # the caller's O need only be 16-byte aligned: the kernels then avoid
+    # their 32-byte stores, with the same bits
+    w = wl.make_workload("al", [700, 1500, 65], s_q=s_q, causal=s_q > 1, seed=41, device="cuda")
+    o_a, l_a = run(w, out_fp32=out_fp32)
+    dt = torch.float32 if out_fp32 else torch.bfloat16
+    n = w.batch * s_q * 128 * 512
+    shift = 16 // torch.empty((), dtype=dt).element_size()
+    base = torch.empty(n + 64, dtype=dt, device="cuda")
+    off = (-(base.data_ptr() // base.element_size()) % (32 // base.element_size())) + shift
+    out = base[off:off + n].view(w.batch, s_q, 128, 512)
+    assert out.data_ptr() % 32 == 16
+    o, l = m.decode_step(w.q, w.kv, w.block_table, w.cache_lens, w.softmax_scale, causal=w.causal,
+                         out_fp32=out_fp32, out=out)
+    torch.cuda.synchronize()
+    assert np.array_equal(o.float().cpu().numpy().astype(np.float64), o_a)
+    assert np.array_equal(l.cpu().numpy().astype(np.float64), l_a)
+
+
 # ---------------------------------------------------------------- split requests and their combine
 
 @pytest.mark.parametrize("s_q,causal,length,units", [(1, False, 64 * 300, 40), (2, True, 128 * 300, 36)])
