@@ -66,6 +66,13 @@
 
 namespace mla {
 
+// 32-byte global store (one whole L2 sector); the address must be 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t* v) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+               ::"l"(p), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
+
 constexpr int kChunkBytes = kPage * 128;         // 64 rows x 64 bf16, 128B-swizzled
 constexpr int kStages = 3;
 constexpr int kStageS = kNumChunks * kChunkBytes;  // 9 chunks: all 576 dims
