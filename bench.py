@@ -230,7 +230,9 @@ def run_reference(args, world, rank):
 
 
 def kernel_name(w) -> str:
-    return "mla_decode_mtp_kernel" if (w.s_q == 2 and not w.topk) else "mla_decode_kernel"
+    # two query tokens over a dense bf16 cache take the paired-SM kernel; an
+    # FP8 cache (and everything else) the one-token kernel
+    return "mla_decode_mtp_kernel" if (w.s_q == 2 and not w.topk and not w.kv_fp8) else "mla_decode_kernel"
 
 
 def time_step(m, w, args, dev, world, sampler=None):
@@ -785,7 +787,7 @@ def main():
     ap.add_argument("--cpu-budget-other", type=float, default=4.0,
                     help="seconds of oracle work for each other workload's CPU baseline")
     ap.add_argument("--also", default="single,uniform_b32,long_b128,sparse_b80,mtp4_b64,"
-                                      "uniform_b32_fp8,long_b128_fp8,sparse_b80_fp8",
+                                      "uniform_b32_fp8,long_b128_fp8,sparse_b80_fp8,mtp_b64_fp8",
                     help="other workloads timed before the headline one (comma-separated; 'none' for none)")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -99,10 +99,11 @@ enum {
                             latent caching in FP8 of "The 31-Millisecond
                             Smoking Gun" (DeepSeek-V4-Flash paragraph) and the
                             precision lever of "How DeepSeek Inference Works".
-                            One-token kernel paths only: every s_q with top-k
-                            lists, and s_q != 2 dense (MLA_ERR_UNSUPPORTED
-                            for s_q = 2 dense).  mla_combine accepts the flag
-                            and ignores it. */
+                            Every s_q, dense or top-k; all run the one-token
+                            kernel (for s_q = 2 dense, one 2-CTA cluster per
+                            token on the plan's two-page tiles, in place of
+                            the paired-SM kernel, which has no FP8 form).
+                            mla_combine accepts the flag and ignores it. */
 };
 
 /*

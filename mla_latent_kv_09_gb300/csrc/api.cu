@@ -27,8 +27,9 @@ int decode_smem_bytes();
 int decode_threads(bool sparse, bool fp8);
 cudaError_t decode_set_attrs();
 cudaError_t decode_max_clusters(int* n, int num_clusters_hint);
-cudaError_t decode_launch(bool sparse, bool fp8, int num_clusters, cudaStream_t stream, const DecodeParams& p,
-                          const CUtensorMap& tm_q, const CUtensorMap& tm_kv, const CUtensorMap& tm_rope);
+cudaError_t decode_launch(bool sparse, bool fp8, bool pair_tiles, int num_clusters, cudaStream_t stream,
+                          const DecodeParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_kv,
+                          const CUtensorMap& tm_rope);
 cudaError_t mtp_set_attrs();
 cudaError_t mtp_max_clusters(int* n, int num_clusters_hint);
 cudaError_t mtp_launch(bool bf16_pv, int num_clusters, cudaStream_t stream, const DecodeParams& p,
@@ -291,8 +292,6 @@ int mla::check_decode_args(const void* q, const void* kv_cache, int64_t num_page
                                      MLA_FLAG_KV_FP8))
     return MLA_ERR_INVALID_ARG;
   if (num_heads != kHeads || s_q < 1 || s_q > MLA_MAX_SQ) return MLA_ERR_UNSUPPORTED;
-  // an FP8 cache runs on the one-token kernel: not the two-token dense path
-  if ((flags & MLA_FLAG_KV_FP8) && plan_tile_rows(s_q, topk) == 128) return MLA_ERR_UNSUPPORTED;
   if (!std::isfinite(softmax_scale) || !(softmax_scale > 0.f)) return MLA_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(out, 16) || !aligned(lse, 4) ||
       !aligned(block_table, 4) || !aligned(cache_lens, 4) || (topk_idx && !aligned(topk_idx, 4)))
@@ -320,7 +319,11 @@ int mla_decode(const void* q, const void* kv_cache, int64_t num_pages, const int
   if (ws_bytes < L.total) return MLA_ERR_WORKSPACE;
   char* ws = static_cast<char*>(workspace);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const bool pair_path = plan_tile_rows(s_q, topk) == 128;
+  // two query tokens over a dense bf16 cache: the paired-SM kernel; an FP8
+  // cache runs the one-token kernel on the same plan (its 128-row tiles
+  // split in two)
+  const bool pair_plan = plan_tile_rows(s_q, topk) == 128;
+  const bool pair_path = pair_plan && !(flags & MLA_FLAG_KV_FP8);
 
   if (flags & MLA_FLAG_VALIDATE) {
     // the check records the first problem in the workspace status word; the
@@ -392,7 +395,7 @@ int mla_decode(const void* q, const void* kv_cache, int64_t num_pages, const int
       return rc;
     e = mtp_launch((flags & MLA_FLAG_BF16_PV) != 0, U, s, p, tm_q, tm_k3, tm_v2, tm_out, tm_part);
   } else {
-    e = decode_launch(topk_idx != nullptr, fp8, U * s_q, s, p, tm_q, tm_kv, tm_rope);
+    e = decode_launch(topk_idx != nullptr, fp8, pair_plan, U * s_q, s, p, tm_q, tm_kv, tm_rope);
   }
   if (e != cudaSuccess) {
     cudaGetLastError();

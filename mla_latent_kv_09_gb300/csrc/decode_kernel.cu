@@ -152,6 +152,34 @@ constexpr uint32_t kIdescQK16 = kIdescQK & ~((1u << 7) | (1u << 10));
 constexpr uint32_t kIdescPV = (1u << 4) | (0u << 7) | (0u << 10) | (1u << 16) | ((256u >> 3) << 17) |
                               ((128u >> 4) << 24);
 
+// The segments of a unit in this kernel's 64-row tiles.  A plan made for
+// two query tokens over a dense cache counts 128-row tiles (kPairTiles: the
+// tiles of the paired-SM kernel, which an FP8 cache does not use): each
+// becomes two, and a segment that ends its request stops at the request's
+// last page.
+template <bool kPairTiles>
+struct Seg64Iter {
+  SegIter it;
+  const int* lens;
+  __device__ Seg64Iter(const DecodeParams& p, int unit) : it(p, unit), lens(p.cache_lens) {}
+  __device__ bool next(Seg& s) {
+    while (it.next(s)) {
+      if (kPairTiles) {
+        const bool to_end = s.t1 == s.n_tiles;
+        s.t0 *= 2;
+        s.t1 *= 2;
+        if (to_end) {
+          const int n64 = (max(lens[s.b], 0) + kPage - 1) / kPage;
+          s.t1 = min(s.t1, n64);
+        }
+        if (s.t0 >= s.t1) continue;
+      }
+      return true;
+    }
+    return false;
+  }
+};
+
 // Position in the 3-deep tile ring.
 struct Ring3 {
   uint32_t idx = 0, phase = 0;
@@ -261,7 +289,7 @@ __host__ __device__ constexpr uint32_t p_message_bytes(bool last) {
   return static_cast<uint32_t>(kPBytes + kHeads * 4 + (last ? kHeads * 4 : 0));
 }
 
-template <bool kSparse, bool kFp8>
+template <bool kSparse, bool kFp8, bool kPairTiles = false>
 __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : (kSparse ? kThreadsSparse : kThreads), 1)
 mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tm_q,
                   const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_rope) {
@@ -365,7 +393,7 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
     const int pair_bar = 1 + q4;  // named barrier of the two warps of this quarter
     // the two warps of a quarter meet at named barriers: they vote there, so
     // that a wait that ran out in one of them makes both leave
-    SegIter it(p, unit);
+    Seg64Iter<kPairTiles> it(p, unit);
     Seg sg;
     uint32_t g = 0, nseg = 0;
     bool ok = true, stop = false;  // ok: this warp's waits so far; stop: the quarter leaves
@@ -516,7 +544,7 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     const volatile float* alpha_s = reinterpret_cast<const volatile float*>(smem + kOffAlpha);
     const volatile float* fin_s = reinterpret_cast<const volatile float*>(smem + kOffFin);
-    SegIter it(p, unit);
+    Seg64Iter<kPairTiles> it(p, unit);
     Seg sg;
     uint32_t g = 0, nseg = 0;
     bool ok = true;
@@ -626,7 +654,7 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
   } else if (warp == 8) {
     // ================================================= MMA issue (one thread)
     if (lane == 0) {
-      SegIter it(p, unit);
+      Seg64Iter<kPairTiles> it(p, unit);
       Seg sg;
       Ring3 rs;
       uint32_t g = 0, nseg = 0;
@@ -712,7 +740,7 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
     // side (dense): one slot per tile, value dims only.  Page ids are read 32
     // at a time with one coalesced load.  (No L2 prefetch from this SM: it
     // would share the TMA unit with the loads and delay them.)
-    SegIter it(p, unit);
+    Seg64Iter<kPairTiles> it(p, unit);
     Seg sg;
     Ring3 rs;
     uint32_t issued = 0;
@@ -775,7 +803,7 @@ mla_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
     // dense: O side warps 4-7, 10-11 convert (ptid 0..191); sparse: S side
     // warps 9-19 (ptid 0..351) and O side warps 4-7, 10-19 (0..447) gather
     const int ptid = s_side ? threadIdx.x - 288 : (warp < 8 ? threadIdx.x - 128 : threadIdx.x - 192);
-    SegIter it(p, unit);
+    Seg64Iter<kPairTiles> it(p, unit);
     Seg sg;
     Ring3 rs;
     bool ok = true;
@@ -1128,6 +1156,7 @@ cudaError_t decode_set_attrs() {
   if (e == cudaSuccess) e = cudaFuncSetAttribute(mla_decode_kernel<true, false>, a, kSmemBytes);
   if (e == cudaSuccess) e = cudaFuncSetAttribute(mla_decode_kernel<false, true>, a, kSmemBytes);
   if (e == cudaSuccess) e = cudaFuncSetAttribute(mla_decode_kernel<true, true>, a, kSmemBytes);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(mla_decode_kernel<false, true, true>, a, kSmemBytes);
   return e;
 }
 
@@ -1161,11 +1190,14 @@ cudaError_t decode_max_clusters(int* n, int num_clusters_hint) {
 // Maps: bf16 cache, tm_kv = a page's nine chunks (S side), tm_rope = its
 // eight value chunks (O side), as 3-D boxes; FP8 cache, tm_kv = each row's
 // 528 latent + scale bytes, tm_rope = its 64 bf16 RoPE dims.
-cudaError_t decode_launch(bool sparse, bool fp8, int num_clusters, cudaStream_t stream, const DecodeParams& p,
-                          const CUtensorMap& tm_q, const CUtensorMap& tm_kv, const CUtensorMap& tm_rope) {
+cudaError_t decode_launch(bool sparse, bool fp8, bool pair_tiles, int num_clusters, cudaStream_t stream,
+                          const DecodeParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_kv,
+                          const CUtensorMap& tm_rope) {
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[2];
   cluster_config(cfg, attr, num_clusters, stream, decode_threads(sparse, fp8), true);
+  if (fp8 && pair_tiles)  // two query tokens over a dense FP8 cache (plan tiles of 128 rows)
+    return cudaLaunchKernelEx(&cfg, mla_decode_kernel<false, true, true>, p, tm_q, tm_kv, tm_rope);
   if (fp8)
     return sparse ? cudaLaunchKernelEx(&cfg, mla_decode_kernel<true, true>, p, tm_q, tm_kv, tm_rope)
                   : cudaLaunchKernelEx(&cfg, mla_decode_kernel<false, true>, p, tm_q, tm_kv, tm_rope);

@@ -79,11 +79,6 @@ def test_null_pointers_and_bad_shapes_are_rejected_before_any_launch(lib):
     assert f(*a) == m.MLA_ERR_INVALID_ARG
     a = list(args); a[12] = 1 << 7  # unknown flag
     assert f(*a) == m.MLA_ERR_INVALID_ARG
-    # an FP8 cache: not on the two-token dense path, which has no FP8 form
-    a = list(args); a[12] = m.MLA_FLAG_KV_FP8; a[7] = 2
-    assert f(*a) == m.MLA_ERR_UNSUPPORTED
-    a = list(args); a[12] = m.MLA_FLAG_KV_FP8 | m.MLA_FLAG_CAUSAL; a[7] = 2
-    assert f(*a) == m.MLA_ERR_UNSUPPORTED
     a = list(args); a[9] = float("nan")
     assert f(*a) == m.MLA_ERR_INVALID_ARG
     assert lib.mla_combine(None, 0, 1, 1, 128, 0, 1, ok_ptr, ok_ptr, None) == m.MLA_ERR_INVALID_ARG

@@ -76,6 +76,7 @@ SMALL = [
     ("long_b128_fp8", dict(batch=3, length=3000)),
     ("sparse_b80_fp8", dict(batch=4, length=5000)),
     ("mtp4_b64_fp8", dict(batch=4, length=700)),
+    ("mtp_b64_fp8", dict(batch=4, length=1500)),
 ]
 
 
@@ -104,7 +105,7 @@ def test_matches_the_bf16_path_on_the_same_values(name):
     assert np.abs(o8 - o16).max() <= 1e-5 and np.abs(l8 - l16).max() <= 1e-5
 
 
-FULL = [("uniform_b32_fp8", 6), ("long_b128_fp8", 3), ("sparse_b80_fp8", 4)]
+FULL = [("uniform_b32_fp8", 6), ("long_b128_fp8", 3), ("sparse_b80_fp8", 4), ("mtp_b64_fp8", 4)]
 
 
 @pytest.mark.parametrize("name,nsample", FULL, ids=[f[0] for f in FULL])
@@ -193,8 +194,13 @@ def test_validate_flags_bad_rows():
     assert _status_of(w, kv) == m.MLA_ERR_VALUE_RANGE
 
 
-def test_two_token_dense_is_unsupported():
-    w = wl.make_config("mtp_b64_fp8", device="cuda", batch=2, length=200)
-    with pytest.raises(m.MlaError) as e:
-        run(w)
-    assert e.value.status == m.MLA_ERR_UNSUPPORTED
+@pytest.mark.parametrize("units", [0, 1, 5])
+def test_two_token_dense_runs_on_two_page_tiles(units):
+    # s_q = 2 over a dense FP8 cache: the one-token kernel on the plan's
+    # 128-row tiles, each split in two; lengths around the tile and page
+    # edges (1, 64, 65, 128, 129, 191), causal, requests split across units
+    lens = [1, 64, 65, 128, 129, 191, 3000, 6000]
+    w = wl.make_workload("f8mtp", lens, s_q=2, causal=True, seed=17, device="cuda", kv_fp8=True)
+    o_ref, lse_ref = reference(w)
+    o, lse = run(w, num_units=units)
+    assert_close(o, lse, o_ref, lse_ref)
