@@ -19,7 +19,7 @@ __global__ void mla_plan_kernel(const int* lens, int B, int topk, int tile_rows,
 __global__ void mla_wait_timeout_kernel(int* status);
 __global__ void mla_combine_kernel(const int* hdr, const int* req_meta, const float* part_lse,
                                    const uint16_t* part_o, int part_bf16, int s_q, int out_fp32, void* out,
-                                   float* lse);
+                                   float* lse, int n_bt);
 __global__ void mla_validate_kernel(const int* lens, const int* bt, long long bt_stride,
                                     long long num_pages, int B, int s_q, const int* topk_idx, int topk,
                                     const uint16_t* kv, int check_range, int* status);
@@ -423,7 +423,9 @@ int mla_combine(void* workspace, size_t ws_bytes, int batch, int s_q, int num_he
   // a programmatic dependent of the decode kernel: scheduled while the decode
   // kernel's last units finish, it waits for that grid before reading
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(batch * s_q, kHeads / 8, 1);
+  // at most one wave: 76 x 16 blocks of 256 threads (8 per SM on 152 SMs),
+  // each block taking every 76th (request, token) row
+  cfg.gridDim = dim3(batch * s_q < 76 ? batch * s_q : 76, kHeads / 8, 1);
   cfg.blockDim = dim3(256, 1, 1);
   cfg.stream = static_cast<cudaStream_t>(stream);
   cudaLaunchAttribute attr[1];
@@ -436,7 +438,7 @@ int mla_combine(void* workspace, size_t ws_bytes, int batch, int s_q, int num_he
                          reinterpret_cast<const int*>(ws + L.reqs),
                          reinterpret_cast<const float*>(ws + L.part_lse),
                          reinterpret_cast<const uint16_t*>(ws + L.part_o), (flags & MLA_FLAG_BF16_PV) ? 1 : 0, s_q,
-                         (flags & MLA_FLAG_OUT_FP32) ? 1 : 0, out, lse);
+                         (flags & MLA_FLAG_OUT_FP32) ? 1 : 0, out, lse, batch * s_q);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return MLA_ERR_CUDA;

@@ -108,118 +108,122 @@ __global__ void __launch_bounds__(1024) mla_plan_kernel(const int* __restrict__ 
 }
 
 // ------------------------------------------------------------------ combine
-// Grid (B * s_q, 128 / 8); warp w of a block merges head blockIdx.y * 8 + w.
+// Grid (min(B * s_q, 76), 128 / 8), one wave of 256-thread blocks on 152
+// SMs: block x takes (request, token) rows x, x + gridDim.x, ..; warp w of
+// a block merges head blockIdx.y * 8 + w.
 // Requests with one split were finished by the decode kernel; requests with
 // no tiles get O = 0, LSE = -inf.
 __global__ void __launch_bounds__(256) mla_combine_kernel(const int* __restrict__ hdr,
                                                           const int* __restrict__ req_meta,
                                                           const float* __restrict__ part_lse,
                                                           const uint16_t* __restrict__ part_o, int part_bf16,
-                                                          int s_q, int out_fp32, void* out, float* lse) {
+                                                          int s_q, int out_fp32, void* out, float* lse, int n_bt) {
   grid_launch_dependents();  // a kernel launched after this one may set up (it waits for this grid)
   grid_dependency_wait();    // the decode kernel has finished (programmatic dependent launch)
   if (hdr[kHdrStatus] != 0) return;  // a failed check or wait: the step's outputs stay unwritten
-  const int bt = blockIdx.x;
-  const int b = bt / s_q, t = bt - b * s_q;
-  const int ns = req_meta[4 * b + 1];
-  if (ns == 1) return;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int h = blockIdx.y * 8 + warp;
-  const long long orow = (static_cast<long long>(bt) * kHeads + h) * kDv;
-  float acc[16];
+  for (int bt = blockIdx.x; bt < n_bt; bt += gridDim.x) {
+    const int b = bt / s_q, t = bt - b * s_q;
+    const int ns = req_meta[4 * b + 1];
+    if (ns == 1) continue;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int h = blockIdx.y * 8 + warp;
+    const long long orow = (static_cast<long long>(bt) * kHeads + h) * kDv;
+    float acc[16];
 #pragma unroll
-  for (int k = 0; k < 16; ++k) acc[k] = 0.f;
-  float LSE = -INFINITY;
-  if (ns > 1) {
-    // Lane s (< 32) holds split s's LSE: one round trip for the LSEs, shuffles
-    // for max, sum and weights, then the partial rows of two splits per
-    // batch (eight 16-byte loads in flight per lane).
-    const int slot0 = req_meta[4 * b + 2];
-    auto lse_of = [&](int s) { return part_lse[(static_cast<long long>(slot0 + s) * s_q + t) * kHeads + h]; };
-    const float lse_l = lane < ns ? lse_of(lane) : -INFINITY;
-    float m = lse_l;
-    for (int s = lane + 32; s < ns; s += 32) m = fmaxf(m, lse_of(s));
+    for (int k = 0; k < 16; ++k) acc[k] = 0.f;
+    float LSE = -INFINITY;
+    if (ns > 1) {
+      // Lane s (< 32) holds split s's LSE: one round trip for the LSEs, shuffles
+      // for max, sum and weights, then the partial rows of two splits per
+      // batch (eight 16-byte loads in flight per lane).
+      const int slot0 = req_meta[4 * b + 2];
+      auto lse_of = [&](int s) { return part_lse[(static_cast<long long>(slot0 + s) * s_q + t) * kHeads + h]; };
+      const float lse_l = lane < ns ? lse_of(lane) : -INFINITY;
+      float m = lse_l;
+      for (int s = lane + 32; s < ns; s += 32) m = fmaxf(m, lse_of(s));
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    if (m != -INFINITY) {
-      float sum = lane < ns ? expf(lse_l - m) : 0.f;
-      for (int s = lane + 32; s < ns; s += 32) sum += expf(lse_of(s) - m);
+      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      if (m != -INFINITY) {
+        float sum = lane < ns ? expf(lse_l - m) : 0.f;
+        for (int s = lane + 32; s < ns; s += 32) sum += expf(lse_of(s) - m);
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-      LSE = m + logf(sum);
-      const float w_l = lane < ns ? expf(lse_l - LSE) : 0.f;
-      // partial rows are 16-bit (fp16, or bf16 with MLA_FLAG_BF16_PV): lane
-      // reads dims {4*lane + 128*k .. +3} as one 8-byte piece per k
-      auto row = [&](int s) {
-        return reinterpret_cast<const uint2*>(part_o + ((static_cast<long long>(slot0 + s) * s_q + t) * kHeads + h) * kDv) + lane;
-      };
-      auto widen = [&](uint2 u) {
-        float4 f;
-        if (part_bf16) {
-          f.x = __uint_as_float(u.x << 16); f.y = __uint_as_float(u.x & 0xffff0000u);
-          f.z = __uint_as_float(u.y << 16); f.w = __uint_as_float(u.y & 0xffff0000u);
-        } else {
-          const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
-          const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
-          f = make_float4(a.x, a.y, b.x, b.y);
+        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        LSE = m + logf(sum);
+        const float w_l = lane < ns ? expf(lse_l - LSE) : 0.f;
+        // partial rows are 16-bit (fp16, or bf16 with MLA_FLAG_BF16_PV): lane
+        // reads dims {4*lane + 128*k .. +3} as one 8-byte piece per k
+        auto row = [&](int s) {
+          return reinterpret_cast<const uint2*>(
+                     part_o + ((static_cast<long long>(slot0 + s) * s_q + t) * kHeads + h) * kDv) + lane;
+        };
+        auto widen = [&](uint2 u) {
+          float4 f;
+          if (part_bf16) {
+            f.x = __uint_as_float(u.x << 16); f.y = __uint_as_float(u.x & 0xffff0000u);
+            f.z = __uint_as_float(u.y << 16); f.w = __uint_as_float(u.y & 0xffff0000u);
+          } else {
+            const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+            const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+            f = make_float4(a.x, a.y, b.x, b.y);
+          }
+          return f;
+        };
+        auto add = [&](float w, const float4 (&v)[4]) {
+          if (w == 0.f) return;  // an empty split adds nothing
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            acc[4 * k + 0] += w * v[k].x; acc[4 * k + 1] += w * v[k].y;
+            acc[4 * k + 2] += w * v[k].z; acc[4 * k + 3] += w * v[k].w;
+          }
+        };
+        const int n32 = ns < 32 ? ns : 32;
+        int s = 0;
+        for (; s + 2 <= n32; s += 2) {
+          const uint2* r0 = row(s);
+          const uint2* r1 = row(s + 1);
+          uint2 u0[4], u1[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            u0[k] = r0[32 * k];
+            u1[k] = r1[32 * k];
+          }
+          float4 v0[4], v1[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            v0[k] = widen(u0[k]);
+            v1[k] = widen(u1[k]);
+          }
+          add(__shfl_sync(0xffffffffu, w_l, s), v0);
+          add(__shfl_sync(0xffffffffu, w_l, s + 1), v1);
         }
-        return f;
-      };
-      auto add = [&](float w, const float4 (&v)[4]) {
-        if (w == 0.f) return;  // an empty split adds nothing
+        for (; s < ns; ++s) {  // the odd split, and splits past 32
+          const float w = s < 32 ? __shfl_sync(0xffffffffu, w_l, s) : expf(lse_of(s) - LSE);
+          const uint2* r0 = row(s);
+          float4 v0[4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          acc[4 * k + 0] += w * v[k].x; acc[4 * k + 1] += w * v[k].y;
-          acc[4 * k + 2] += w * v[k].z; acc[4 * k + 3] += w * v[k].w;
+          for (int k = 0; k < 4; ++k) v0[k] = widen(r0[32 * k]);
+          add(w, v0);
         }
-      };
-      const int n32 = ns < 32 ? ns : 32;
-      int s = 0;
-      for (; s + 2 <= n32; s += 2) {
-        const uint2* r0 = row(s);
-        const uint2* r1 = row(s + 1);
-        uint2 u0[4], u1[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          u0[k] = r0[32 * k];
-          u1[k] = r1[32 * k];
-        }
-        float4 v0[4], v1[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          v0[k] = widen(u0[k]);
-          v1[k] = widen(u1[k]);
-        }
-        add(__shfl_sync(0xffffffffu, w_l, s), v0);
-        add(__shfl_sync(0xffffffffu, w_l, s + 1), v1);
-      }
-      for (; s < ns; ++s) {  // the odd split, and splits past 32
-        const float w = s < 32 ? __shfl_sync(0xffffffffu, w_l, s) : expf(lse_of(s) - LSE);
-        const uint2* r0 = row(s);
-        float4 v0[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) v0[k] = widen(r0[32 * k]);
-        add(w, v0);
       }
     }
-  }
-  // lane covers dims {4*lane + 128*k .. +3}, k = 0..3 (coalesced 16-byte pieces)
-  if (out_fp32) {
-    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out) + orow) + lane;
+    // lane covers dims {4*lane + 128*k .. +3}, k = 0..3 (coalesced 16-byte pieces)
+    if (out_fp32) {
+      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out) + orow) + lane;
 #pragma unroll
-    for (int k = 0; k < 4; ++k)
-      dst[32 * k] = make_float4(acc[4 * k], acc[4 * k + 1], acc[4 * k + 2], acc[4 * k + 3]);
-  } else {
-    uint2* dst = reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + orow) + lane;
+      for (int k = 0; k < 4; ++k)
+        dst[32 * k] = make_float4(acc[4 * k], acc[4 * k + 1], acc[4 * k + 2], acc[4 * k + 3]);
+    } else {
+      uint2* dst = reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + orow) + lane;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      uint32_t lo, hi;
-      asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(lo) : "f"(acc[4 * k + 1]), "f"(acc[4 * k]));
-      asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(hi) : "f"(acc[4 * k + 3]), "f"(acc[4 * k + 2]));
-      dst[32 * k] = make_uint2(lo, hi);
+      for (int k = 0; k < 4; ++k) {
+        uint32_t lo, hi;
+        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(lo) : "f"(acc[4 * k + 1]), "f"(acc[4 * k]));
+        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(hi) : "f"(acc[4 * k + 3]), "f"(acc[4 * k + 2]));
+        dst[32 * k] = make_uint2(lo, hi);
+      }
     }
+    if (lane == 0) lse[static_cast<long long>(bt) * kHeads + h] = LSE;
   }
-  if (lane == 0) lse[static_cast<long long>(bt) * kHeads + h] = LSE;
 }
 
 // ------------------------------------------------------------------ validate
