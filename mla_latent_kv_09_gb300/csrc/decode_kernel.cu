@@ -57,6 +57,10 @@
 // O side 4-7 and 10-19; the MMA thread waits for the fill threads' arrivals
 // (kVR) on every ring slot, Q slots included.  (The fill work is latency-
 // bound: 20 warps, so that 10-14 of them fill, measured faster than 16.)
+// Two query tokens over a dense FP8 cache (which the paired-SM two-token
+// kernel does not read) run here too, one cluster per token, on the plan
+// the paired-SM kernel would get: the kPairTiles instance splits each of its
+// 128-row tiles into two of this kernel's 64-row tiles (Seg64Iter).
 #include <cuda_runtime.h>
 
 #include "common.cuh"
