@@ -26,12 +26,13 @@ def _build():
     assert torch.cuda.is_available()
 
 
-def run(w, kv=None, table=None, out_fp32=True, num_units=0, validate=False):
+def run(w, kv=None, table=None, out_fp32=True, num_units=0, validate=False, bf16_pv=False):
     ws = m.Workspace(w.batch, w.s_q, num_units, w.q.device)
     ws.buf.fill_(0x7F)  # nothing the step leaves unwritten may pass as a result
     o, lse = m.decode_step(w.q, w.kv if kv is None else kv, w.block_table if table is None else table,
                            w.cache_lens, w.softmax_scale, causal=w.causal, topk_idx=w.topk_idx,
-                           out_fp32=out_fp32, num_units=num_units, validate=validate, workspace=ws)
+                           out_fp32=out_fp32, num_units=num_units, validate=validate, bf16_pv=bf16_pv,
+                           workspace=ws)
     torch.cuda.synchronize()
     assert m.mla_workspace_status(ws.buf) == m.MLA_OK  # no device wait ran out
     return o.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64)
@@ -203,4 +204,14 @@ def test_two_token_dense_runs_on_two_page_tiles(units):
     w = wl.make_workload("f8mtp", lens, s_q=2, causal=True, seed=17, device="cuda", kv_fp8=True)
     o_ref, lse_ref = reference(w)
     o, lse = run(w, num_units=units)
+    assert_close(o, lse, o_ref, lse_ref)
+
+
+def test_two_token_dense_with_bf16_partials():
+    # MLA_FLAG_BF16_PV on this path only stores split requests' partial rows
+    # in bf16 (8 significant bits, read back by the combine as bf16): the
+    # bar holds with split requests
+    w = wl.make_workload("f8mtpb", [5000, 3000, 700], s_q=2, causal=True, seed=19, device="cuda", kv_fp8=True)
+    o_ref, lse_ref = reference(w)
+    o, lse = run(w, bf16_pv=True)
     assert_close(o, lse, o_ref, lse_ref)
