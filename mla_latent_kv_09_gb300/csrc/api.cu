@@ -241,7 +241,9 @@ int mla_decode_plan(const int32_t* cache_lens, int batch, int s_q, int topk, int
   const WsLayout L = ws_layout(batch, s_q, U);
   if (ws_bytes < L.total) return MLA_ERR_WORKSPACE;
   char* ws = static_cast<char*>(workspace);
-  mla_plan_kernel<<<1, 1024, 0, static_cast<cudaStream_t>(stream)>>>(
+  // up to 128 requests (every decode batch the bench times) one 128-thread
+  // CTA: its block scans meet at fewer warps (~1 us off each call)
+  mla_plan_kernel<<<1, batch <= 128 ? 128 : 1024, 0, static_cast<cudaStream_t>(stream)>>>(
       cache_lens, batch, topk, plan_tile_rows(s_q, topk), U, reinterpret_cast<int*>(ws + L.hdr),
       reinterpret_cast<int*>(ws + L.units), reinterpret_cast<int*>(ws + L.reqs), L.slots);
   return last_cuda_error();

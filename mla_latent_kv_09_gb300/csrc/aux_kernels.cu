@@ -14,7 +14,7 @@ namespace mla {
 
 // ------------------------------------------------------------------ plan
 constexpr int kPlanSmemReqs = 4096;  // requests whose cost prefix the plan keeps in shared memory
-// Block-wide inclusive scan of one int per thread (1024 threads).
+// Block-wide inclusive scan of one int per thread (up to 1024 threads).
 __device__ int block_inclusive_scan(int v, int* s_warp, int& total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
@@ -40,7 +40,8 @@ __device__ int block_inclusive_scan(int v, int* s_warp, int& total) {
   return res;
 }
 
-// One CTA of 1024 threads.  Step 1: tiles and cost prefix per request.
+// One CTA (128 threads up to 128 requests, else 1024).  Step 1: tiles and
+// cost prefix per request.
 // Step 2: split count and first partial slot per request.  Step 3: the
 // (request, tile) range of every unit, by binary search over the cost
 // prefixes (kept in shared memory when they fit: the searches are chains of
